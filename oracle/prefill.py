@@ -1,0 +1,115 @@
+"""The grouped MoE prefill layer on FP16 operands (oracle; test infrastructure only).
+
+What is computed (#2356 Summary: prompt rows sorted by expert, IQ4_NL weights
+dequantised to FP16 for the tensor cores with FP32 sums; #1525 Change: each
+dequantised value is one expression rounded by ``__float2half_rn``, SwiGLU
+between the two products, the top-k outputs combined):
+
+    ids, w  = top-k of the router logits, softmax over the k (as in decode)
+    order   = the (token, slot) entries sorted by expert, ties by entry index
+    Xh      = fp16_rn(x)                          x given as BF16
+    Wh      = fp16_rn(fp32(d) * kvalues[idx])     one rounding of an exact product
+    g, u    = Wh_gu[e] . Xh[t]                    here in float64
+    H       = fp16_rn(silu(g) * u)                H is FP16, the second GEMM's input
+    o       = Wh_dn[e] . H                        float64
+    out[t]  = sum_{k ascending} w[t, k] * o[(t, k)]
+
+Readings (pages silent): H is rounded to FP16 once from the exact value; the
+sort is stable by token, which does not change any result.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import formats
+from . import moe as _moe
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """BF16 bit patterns to FP32 (exact)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32)
+
+
+def fp16_rn(x: np.ndarray) -> np.ndarray:
+    """Round to FP16, nearest even, straight from the given precision."""
+    return np.asarray(x).astype(np.float16)
+
+
+def dequant_fp16(fmt: str, blocks: np.ndarray) -> np.ndarray:
+    """fp16_rn(fp32(d) * q) as float16 [rows, K].  The FP32 product is exact
+    (11-bit scale significand times a 7-bit integer), so this is one rounding."""
+    d, q = formats.decode(fmt, blocks)
+    rows, nb = d.shape
+    prod32 = (np.repeat(d.astype(np.float32), 32, axis=1) * q.astype(np.float32))
+    return fp16_rn(prod32.reshape(rows, nb * 32))
+
+
+def sort_entries(ids: np.ndarray, n_experts: int):
+    """Entries t*k+slot sorted by expert, ties by entry index (stable).
+
+    Returns (order int64 [T*k], offsets int64 [n_experts+1])."""
+    flat = np.asarray(ids, dtype=np.int64).reshape(-1)
+    order = np.argsort(flat, kind='stable')
+    counts = np.bincount(flat, minlength=n_experts)
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    return order, offsets
+
+
+class ExpertCache:
+    """Dequantised FP16 experts, built on first use."""
+
+    def __init__(self, fmt: str, blocks_of):
+        self.fmt, self.blocks_of, self.cache = fmt, blocks_of, {}
+
+    def __getitem__(self, e: int) -> np.ndarray:
+        if e not in self.cache:
+            self.cache[e] = dequant_fp16(self.fmt, self.blocks_of[e]).astype(np.float64)
+        return self.cache[e]
+
+
+def moe_prefill(gate_up, down, x_bf16: np.ndarray, ids: np.ndarray, w: np.ndarray,
+                tokens=None, fmt: str = "iq4_nl", h_override=None):
+    """Prefill output rows for ``tokens`` (default: every token).
+
+    gate_up[e]: GGUF blocks [2*inter, hidden/32, *]; down[e]: [hidden, inter/32, *].
+    x_bf16: uint16 [T, hidden].  ids, w: [T, k].
+    ``h_override(t, slot)`` may return an FP16 H row that replaces the oracle's
+    (the tests use it to check the second product on the GPU's own H).
+
+    Returns dict: tokens, out [n, hidden] float64, out_A (error scale),
+    g, u, H (float16) [n, k, inter] and gu_A [n, k, 2*inter]."""
+    T, hidden = x_bf16.shape
+    k = ids.shape[1]
+    if tokens is None:
+        tokens = list(range(T))
+    Wgu = ExpertCache(fmt, gate_up)
+    Wdn = ExpertCache(fmt, down)
+    inter = Wgu[int(ids[tokens[0], 0])].shape[0] // 2
+    n = len(tokens)
+    out = np.zeros((n, hidden))
+    out_A = np.zeros((n, hidden))
+    G = np.zeros((n, k, inter))
+    U = np.zeros((n, k, inter))
+    Hs = np.zeros((n, k, inter), dtype=np.float16)
+    gu_A = np.zeros((n, k, 2 * inter))
+    for i, t in enumerate(tokens):
+        xh = fp16_rn(bf16_bits_to_f32(x_bf16[t])).astype(np.float64)
+        for s in range(k):
+            e = int(ids[t, s])
+            wg = Wgu[e]
+            gu = wg @ xh
+            gu_A[i, s] = np.abs(wg) @ np.abs(xh)
+            G[i, s], U[i, s] = gu[:inter], gu[inter:]
+            if h_override is not None:
+                h = np.asarray(h_override(t, s), dtype=np.float16)
+            else:
+                h = fp16_rn(_moe.silu(gu[:inter]) * gu[inter:])
+            Hs[i, s] = h
+            wd = Wdn[e]
+            hf = h.astype(np.float64)
+            o = wd @ hf
+            oA = np.abs(wd) @ np.abs(hf)
+            out[i] += float(w[t, s]) * o
+            out_A[i] += abs(float(w[t, s])) * oA
+    return dict(tokens=tokens, out=out, out_A=out_A, g=G, u=U, H=Hs, gu_A=gu_A)
