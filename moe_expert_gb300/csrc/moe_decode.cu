@@ -1,0 +1,637 @@
+// The grouped MoE decode layer: grouped gate/up GEMV with SwiGLU + q8_1 of H
+// fused into its epilogue, then the grouped down GEMV with the weighted top-k
+// combine fused into its epilogue (#242 What it does: native_gu_kernel /
+// native_down_kernel over every entry of an expert group; #1525 Change:
+// swiglu_quant and the moe_combine sum in slot order).
+//
+// Two kernels, no host synchronisation:
+//  1. gate/up: every CTA rebuilds the expert groups from the routing ids and
+//     quantises the layer input (both tiny), then streams work units of one
+//     expert x 32 intermediate indices (32 gate rows + the 32 matching up
+//     rows), so the SwiGLU and the 32-value q8_1 block of H are finished in
+//     the CTA; H itself is never stored, only Hq (workspace).
+//  2. down: every CTA owns a contiguous range of output rows across all the
+//     routed experts, so it can form out[t] = sum_k w[t,k] * o[(t,k)] for its
+//     rows in slot order without any cross-CTA reduction.  Its weight stream
+//     depends only on the routing, so it starts before the gate/up kernel has
+//     finished (programmatic dependent launch); Hq is read after
+//     griddepcontrol.wait.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "gemv_core.cuh"
+#include "internal.h"
+
+namespace moex {
+
+constexpr int MAX_ENTRIES = 64;   // T * k
+constexpr int MAX_TOKENS = 8;
+constexpr int MAX_GROUP = 8;      // entries per pass of one expert
+
+struct DecodeArgs {
+  // gate/up stack [E][2I][H]
+  const uint8_t* gu_qs;
+  const uint8_t* gu_sc;
+  int gu_qrow, gu_scrow;
+  // down stack [E][H][I]
+  const uint8_t* dn_qs;
+  const uint8_t* dn_sc;
+  int dn_qrow, dn_scrow;
+  int H, I, E, T, k, n;
+  const float* x;
+  const int32_t* ids;
+  const float* w;
+  float* out;
+  int8_t* hq;      // [n][I]
+  float* hds;      // [n][I/32][2]
+  float* gu_dbg;
+  float* h_dbg;
+  int8_t* hq_dbg;
+  float* hds_dbg;
+  uint32_t* status;
+  int nst, stage_bytes;
+};
+
+// Expert groups of the routing entries: group g holds entries
+// ent[gstart[g] .. gstart[g+1]) (ascending entry index) of expert gexp[g];
+// experts ascending; an expert with more than MAX_GROUP entries gets several
+// consecutive groups.  Entries with an id outside [0, E) are left out and
+// flagged.
+struct Groups {
+  int ng;
+  int gexp[MAX_ENTRIES];
+  int gstart[MAX_ENTRIES + 1];
+  int ent[MAX_ENTRIES];
+};
+
+__device__ void build_groups(Groups& G, const int32_t* ids, int n, int E, uint32_t* status) {
+  int m = 0;
+  for (int j = 0; j < n; ++j) {
+    const int e = ids[j];
+    if (e < 0 || e >= E) {
+      flag_status(status, DEV_BAD_ROUTE);
+      continue;
+    }
+    // insertion by (expert, entry)
+    int p = m;
+    while (p > 0 && ids[G.ent[p - 1]] > e) {
+      G.ent[p] = G.ent[p - 1];
+      --p;
+    }
+    G.ent[p] = j;
+    ++m;
+  }
+  int ng = 0;
+  for (int p = 0; p < m; ++p) {
+    const int e = ids[G.ent[p]];
+    if (ng == 0 || G.gexp[ng - 1] != e || p - G.gstart[ng - 1] >= MAX_GROUP) {
+      G.gexp[ng] = e;
+      G.gstart[ng] = p;
+      ++ng;
+    }
+  }
+  G.gstart[ng] = m;
+  G.ng = ng;
+}
+
+// ============================================================== gate / up
+
+struct GuSmem {
+  int bars, cnt, ucnt, abort_flag, groups, xs, xd, red, ubuf, stages, total;
+  int nub;
+  __host__ __device__ GuSmem(int T, int H, int NS, int nst, int stage_bytes) {
+    nub = nst / 8 + 2;
+    const int NB = H / QK;
+    int o = 0;
+    bars = o; o += 16 * nst;
+    cnt = o; o += 4 * nst;
+    ucnt = o; o += 4 * nub;
+    abort_flag = o; o += 16;
+    o = (o + 15) & ~15;
+    groups = o; o += static_cast<int>(sizeof(Groups));
+    o = (o + 15) & ~15;
+    xs = o; o += T * H;
+    o = (o + 15) & ~15;
+    xd = o; o += 4 * T * NB;
+    o = (o + 15) & ~15;
+    red = o; o += 4 * nst * SR * NS * MAX_GROUP;
+    ubuf = o; o += 4 * nub * 64 * MAX_GROUP;
+    o = (o + 127) & ~127;
+    stages = o; o += nst * stage_bytes;
+    total = o;
+  }
+};
+
+// SwiGLU + q8_1 of one 32-index block of H for C entries, by one warp:
+// lane i takes element i; amax and sum(q) are exact warp reductions, so the
+// block is the same as q8_1_block on the same H values.
+template <int C>
+__device__ __forceinline__ void gu_epilogue(const DecodeArgs& a, const Groups& G, int g, int ib, const float* ub,
+                                            int lane) {
+  const int base = G.gstart[g];
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    const int j = G.ent[base + c];
+    const float gv = ub[lane * MAX_GROUP + c];
+    const float uv = ub[(32 + lane) * MAX_GROUP + c];
+    const float silu = __fdiv_rn(gv, 1.0f + expf(-gv));
+    const float h = __fmul_rn(silu, uv);
+    float amax = fabsf(h);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const int q = amax > 0.f ? static_cast<int>(roundf(__fdiv_rn(h, d))) : 0;
+    int sum = q;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const int i = ib * QK + lane;
+    a.hq[static_cast<int64_t>(j) * a.I + i] = static_cast<int8_t>(q);
+    const float dd = amax > 0.f ? d : 0.f;
+    const float ss = amax > 0.f ? __fmul_rn(d, static_cast<float>(sum)) : 0.f;
+    if (lane == 0) reinterpret_cast<float2*>(a.hds)[static_cast<int64_t>(j) * (a.I / QK) + ib] = make_float2(dd, ss);
+    if (a.gu_dbg) {
+      a.gu_dbg[static_cast<int64_t>(j) * 2 * a.I + i] = gv;
+      a.gu_dbg[static_cast<int64_t>(j) * 2 * a.I + a.I + i] = uv;
+    }
+    if (a.h_dbg) a.h_dbg[static_cast<int64_t>(j) * a.I + i] = h;
+    if (a.hq_dbg) a.hq_dbg[static_cast<int64_t>(j) * a.I + i] = static_cast<int8_t>(q);
+    if (a.hds_dbg && lane == 0)
+      reinterpret_cast<float2*>(a.hds_dbg)[static_cast<int64_t>(j) * (a.I / QK) + ib] = make_float2(dd, ss);
+  }
+}
+
+// One work unit (group g, intermediate block ib): 8 stages of 8 rows.
+template <int C, int WPS>
+__device__ __forceinline__ void gu_unit(const DecodeArgs& a, const Groups& G, int g, int ib, int ui, int NB, int NS,
+                                        int nwc, const ConsumerPos& pos, const int8_t* xs, const float* xd,
+                                        uint64_t* full, uint64_t* empty, int* cnt, int* ucnt, float* red, float* ubuf,
+                                        int nub, const uint8_t* stages, volatile int* abort_flag, bool& dead) {
+  ActRegs<MOEX_Q8_0, C> act;
+  {
+    const int8_t* xcol[C];
+    const float* dcol[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      const int t = G.ent[G.gstart[g] + c] / a.k;
+      xcol[c] = xs + t * a.H;
+      dcol[c] = xd + t * NB;
+    }
+    const int b = pos.ks * SLICE + pos.li;
+    load_act<MOEX_Q8_0, C>(act, xcol, dcol, b, b < NB, pos.li);
+  }
+  float* ub = ubuf + (ui % nub) * 64 * MAX_GROUP;
+  for (int s = 0; s < 8; ++s) {
+    const int it = ui * 8 + s;
+    const int slot = it % a.nst;
+    if (!dead && !mbar_wait(&full[slot], (it / a.nst) & 1, abort_flag)) {
+      if (pos.lane == 0) {
+        *abort_flag = 1;
+        flag_status(a.status, DEV_TIMEOUT_PIPE);
+      }
+      dead = true;
+    }
+    if (dead) continue;
+    const uint8_t* stage = stages + static_cast<size_t>(slot) * a.stage_bytes;
+    float* rs = red + slot * (SR * NS * MAX_GROUP);
+    stage_partials<MOEX_Q8_0, C, WPS>(stage, stage + SR * a.gu_qrow, a.gu_qrow, a.gu_scrow, SR, NB, NS, pos, act,
+                                      rs);
+    if (stage_arrive_last(&cnt[slot], nwc, pos.lane)) {
+      stage_final<C>(rs, SR, NS, pos.lane,
+                     [&](int row, int c, float v) { ub[(s * SR + row) * MAX_GROUP + c] = v; });
+      if (pos.lane == 0) cnt[slot] = 0;
+      // unit completion
+      int old = 0;
+      __syncwarp();
+      if (pos.lane == 0) {
+        __threadfence_block();
+        old = atomicAdd(&ucnt[ui % nub], 1);
+      }
+      old = __shfl_sync(0xffffffffu, old, 0);
+      if (old == 7) {
+        __threadfence_block();
+        gu_epilogue<C>(a, G, g, ib, ub, pos.lane);
+        if (pos.lane == 0) ucnt[ui % nub] = 0;
+      }
+      __syncwarp();
+    }
+    if (pos.lane == 0) mbar_arrive(&empty[slot]);
+  }
+}
+
+template <int WPS>
+__global__ void __launch_bounds__(512, 1) moe_gu_kernel(DecodeArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int NB = a.H / QK;
+  const int NS = num_slices(NB);
+  const GuSmem L(a.T, a.H, NS, a.nst, a.stage_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + a.nst;
+  int* cnt = reinterpret_cast<int*>(smem + L.cnt);
+  int* ucnt = reinterpret_cast<int*>(smem + L.ucnt);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+  Groups& G = *reinterpret_cast<Groups*>(smem + L.groups);
+  int8_t* xs = reinterpret_cast<int8_t*>(smem + L.xs);
+  float* xd = reinterpret_cast<float*>(smem + L.xd);
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  float* ubuf = reinterpret_cast<float*>(smem + L.ubuf);
+  uint8_t* stages = smem + L.stages;
+
+  const int nwc = NS * WPS;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.nst; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], nwc);
+      cnt[i] = 0;
+    }
+    for (int i = 0; i < L.nub; ++i) ucnt[i] = 0;
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  pdl_wait();  // routing ids and the layer input come from earlier kernels
+  if (threadIdx.x == 0) build_groups(G, a.ids, a.n, a.E, a.status);
+  // q8_1 of the layer input (same block arithmetic as quantize_q8_1)
+  for (int t = threadIdx.x; t < a.T * NB; t += blockDim.x) {
+    const int tok = t / NB, b = t % NB;
+    float v[QK];
+    const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<int64_t>(tok) * a.H + b * QK);
+#pragma unroll
+    for (int i = 0; i < QK / 4; ++i) {
+      const float4 f = src[i];
+      v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+    }
+    uint32_t qw[8];
+    float d, s;
+    q8_1_block(v, qw, &d, &s);
+    uint4* dst = reinterpret_cast<uint4*>(xs + tok * a.H + b * QK);
+    dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+    dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+    xd[tok * NB + b] = d;
+  }
+  __syncthreads();
+  pdl_launch_dependents();  // after the wait: the routing ids are complete
+
+  const int ib_per = a.I / QK;
+  const int units = G.ng * ib_per;
+  const int nunit = units > static_cast<int>(blockIdx.x) ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+
+  if (warp == nwc) {
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      int issued = 0;
+      for (int ui = 0; ui < nunit && !*abort_flag; ++ui) {
+        const int u = blockIdx.x + ui * gridDim.x;
+        const int g = u / ib_per, ib = u % ib_per;
+        const int64_t mat_row0 = static_cast<int64_t>(G.gexp[g]) * 2 * a.I;
+        for (int s = 0; s < 8; ++s) {
+          const int it = ui * 8 + s;
+          const int slot = it % a.nst;
+          if (it >= a.nst && !mbar_wait(&empty[slot], ((it / a.nst) - 1) & 1, abort_flag)) {
+            *abort_flag = 1;
+            flag_status(a.status, DEV_TIMEOUT_PIPE);
+            break;
+          }
+          const int64_t r0 = mat_row0 + (s < 4 ? ib * QK + s * SR : a.I + ib * QK + (s - 4) * SR);
+          uint8_t* st = stages + static_cast<size_t>(slot) * a.stage_bytes;
+          mbar_arrive_expect_tx(&full[slot], SR * (a.gu_qrow + a.gu_scrow));
+          bulk_g2s_stream(st, a.gu_qs + r0 * a.gu_qrow, SR * a.gu_qrow, &full[slot], pol);
+          bulk_g2s_stream(st + SR * a.gu_qrow, a.gu_sc + r0 * a.gu_scrow, SR * a.gu_scrow, &full[slot], pol);
+          issued = it + 1;
+        }
+      }
+      if (*abort_flag) {
+        for (int it = max(0, issued - a.nst); it < issued; ++it)
+          mbar_wait(&full[it % a.nst], (it / a.nst) & 1, nullptr);
+      }
+    }
+    return;
+  }
+
+  ConsumerPos pos;
+  pos.ks = warp / WPS;
+  pos.jw = warp % WPS;
+  pos.lane = lane;
+  pos.hf = lane >> 4;
+  pos.li = lane & 15;
+  bool dead = false;
+  for (int ui = 0; ui < nunit; ++ui) {
+    const int u = blockIdx.x + ui * gridDim.x;
+    const int g = u / ib_per, ib = u % ib_per;
+    const int m = G.gstart[g + 1] - G.gstart[g];
+    switch (m) {
+      case 1: gu_unit<1, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
+      case 2: gu_unit<2, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
+      case 3: gu_unit<3, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
+      case 4: gu_unit<4, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
+      case 5: gu_unit<5, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
+      case 6: gu_unit<6, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
+      case 7: gu_unit<7, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
+      default: gu_unit<8, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
+    }
+  }
+}
+
+// ============================================================== down + combine
+
+struct DnSmem {
+  int bars, cnt, abort_flag, groups, hs, hd, red, osum, stages, total;
+  __host__ __device__ DnSmem(int n, int I, int NS, int rows_max, int nst, int stage_bytes) {
+    const int NB = I / QK;
+    int o = 0;
+    bars = o; o += 16 * nst;
+    cnt = o; o += 4 * nst;
+    abort_flag = o; o += 16;
+    o = (o + 15) & ~15;
+    groups = o; o += static_cast<int>(sizeof(Groups));
+    o = (o + 15) & ~15;
+    hs = o; o += n * I;
+    o = (o + 15) & ~15;
+    hd = o; o += 4 * n * NB;
+    o = (o + 15) & ~15;
+    red = o; o += 4 * nst * SR * NS * MAX_GROUP;
+    osum = o; o += 4 * n * rows_max;
+    o = (o + 127) & ~127;
+    stages = o; o += nst * stage_bytes;
+    total = o;
+  }
+};
+
+// Stages of one group: the CTA's nrows rows split into ceil(nrows/8) stages
+// of balanced size; stage s covers rows [s*nrows/ns, (s+1)*nrows/ns).
+__device__ __forceinline__ int dn_nstages(int nrows) { return (nrows + SR - 1) / SR; }
+
+template <int FMT, int C, int WPS>
+__device__ __forceinline__ void dn_group(const DecodeArgs& a, const Groups& G, int g, int it0, int nrows, int NB,
+                                         int NS, int nwc, const ConsumerPos& pos, const int8_t* hs, const float* hd,
+                                         uint64_t* full, uint64_t* empty, int* cnt, float* red, float* osum,
+                                         int rows_max, const uint8_t* stages, volatile int* abort_flag, bool& dead) {
+  ActRegs<FMT, C> act;
+  {
+    const int8_t* xcol[C];
+    const float* dcol[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      const int j = G.ent[G.gstart[g] + c];
+      xcol[c] = hs + j * a.I;
+      dcol[c] = hd + j * NB;
+    }
+    const int b = pos.ks * SLICE + pos.li;
+    load_act<FMT, C>(act, xcol, dcol, b, b < NB, pos.li);
+  }
+  const int ns = dn_nstages(nrows);
+  for (int s = 0; s < ns; ++s) {
+    const int it = it0 + s;
+    const int slot = it % a.nst;
+    if (!dead && !mbar_wait(&full[slot], (it / a.nst) & 1, abort_flag)) {
+      if (pos.lane == 0) {
+        *abort_flag = 1;
+        flag_status(a.status, DEV_TIMEOUT_PIPE);
+      }
+      dead = true;
+    }
+    if (dead) continue;
+    const int rlo = s * nrows / ns, rhi = (s + 1) * nrows / ns;
+    const uint8_t* stage = stages + static_cast<size_t>(slot) * a.stage_bytes;
+    float* rs = red + slot * (SR * NS * MAX_GROUP);
+    stage_partials<FMT, C, WPS>(stage, stage + SR * a.dn_qrow, a.dn_qrow, a.dn_scrow, rhi - rlo, NB, NS, pos, act,
+                                rs);
+    if (stage_arrive_last(&cnt[slot], nwc, pos.lane)) {
+      const int gbase = G.gstart[g];
+      stage_final<C>(rs, rhi - rlo, NS, pos.lane, [&](int row, int c, float v) {
+        osum[G.ent[gbase + c] * rows_max + rlo + row] = v;
+      });
+      if (pos.lane == 0) cnt[slot] = 0;
+      __syncwarp();
+    }
+    if (pos.lane == 0) mbar_arrive(&empty[slot]);
+  }
+}
+
+template <int FMT, int WPS>
+__global__ void __launch_bounds__(512, 1) moe_dn_kernel(DecodeArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int NB = a.I / QK;
+  const int NS = num_slices(NB);
+  const int G_ = gridDim.x;
+  const int rows_max = (a.H + G_ - 1) / G_;
+  const DnSmem L(a.n, a.I, NS, rows_max, a.nst, a.stage_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + a.nst;
+  int* cnt = reinterpret_cast<int*>(smem + L.cnt);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+  Groups& G = *reinterpret_cast<Groups*>(smem + L.groups);
+  int8_t* hs = reinterpret_cast<int8_t*>(smem + L.hs);
+  float* hd = reinterpret_cast<float*>(smem + L.hd);
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  float* osum = reinterpret_cast<float*>(smem + L.osum);
+  const uint8_t* stages = smem + L.stages;
+
+  const int nwc = NS * WPS;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row_begin = static_cast<int>(static_cast<int64_t>(a.H) * blockIdx.x / G_);
+  const int row_end = static_cast<int>(static_cast<int64_t>(a.H) * (blockIdx.x + 1) / G_);
+  const int nrows = row_end - row_begin;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.nst; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], nwc);
+      cnt[i] = 0;
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    // The routing ids were complete before the gate/up kernel let this grid
+    // launch, so they are read before griddepcontrol.wait.
+    build_groups(G, a.ids, a.n, a.E, nullptr);
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  if (warp == nwc) {
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      const int ns = dn_nstages(nrows);
+      int it = 0, issued = 0;
+      for (int g = 0; g < G.ng && !*abort_flag; ++g) {
+        const int64_t mat_row0 = static_cast<int64_t>(G.gexp[g]) * a.H + row_begin;
+        for (int s = 0; s < ns; ++s, ++it) {
+          const int slot = it % a.nst;
+          if (it >= a.nst && !mbar_wait(&empty[slot], ((it / a.nst) - 1) & 1, abort_flag)) {
+            *abort_flag = 1;
+            flag_status(a.status, DEV_TIMEOUT_PIPE);
+            break;
+          }
+          const int rlo = s * nrows / ns, rhi = (s + 1) * nrows / ns;
+          const int64_t r0 = mat_row0 + rlo;
+          const int n = rhi - rlo;
+          uint8_t* st = const_cast<uint8_t*>(stages) + static_cast<size_t>(slot) * a.stage_bytes;
+          mbar_arrive_expect_tx(&full[slot], n * (a.dn_qrow + a.dn_scrow));
+          bulk_g2s_stream(st, a.dn_qs + r0 * a.dn_qrow, n * a.dn_qrow, &full[slot], pol);
+          bulk_g2s_stream(st + SR * a.dn_qrow, a.dn_sc + r0 * a.dn_scrow, n * a.dn_scrow, &full[slot], pol);
+          issued = it + 1;
+        }
+      }
+      if (*abort_flag) {
+        for (int i = max(0, issued - a.nst); i < issued; ++i) mbar_wait(&full[i % a.nst], (i / a.nst) & 1, nullptr);
+      }
+    }
+    return;
+  }
+
+  // consumers: Hq of every entry into shared memory, after the gate/up grid
+  pdl_wait();
+  const int nthr = nwc * 32;
+  {
+    const int4* src = reinterpret_cast<const int4*>(a.hq);
+    int4* dst = reinterpret_cast<int4*>(hs);
+    for (int i = threadIdx.x; i < a.n * a.I / 16; i += nthr) dst[i] = src[i];
+    const float2* dsrc = reinterpret_cast<const float2*>(a.hds);
+    for (int i = threadIdx.x; i < a.n * NB; i += nthr) hd[i] = dsrc[i].x;
+    for (int i = threadIdx.x; i < a.n * rows_max; i += nthr) osum[i] = 0.f;
+    named_bar_sync(1, nthr);
+  }
+  ConsumerPos pos;
+  pos.ks = warp / WPS;
+  pos.jw = warp % WPS;
+  pos.lane = lane;
+  pos.hf = lane >> 4;
+  pos.li = lane & 15;
+  bool dead = false;
+  const int ns = dn_nstages(nrows);
+  for (int g = 0; g < G.ng; ++g) {
+    const int m = G.gstart[g + 1] - G.gstart[g];
+    const int it0 = g * ns;
+#define MOEX_DN(CC) \
+  dn_group<FMT, CC, WPS>(a, G, g, it0, nrows, NB, NS, nwc, pos, hs, hd, full, empty, cnt, red, osum, rows_max, stages, abort_flag, dead)
+    switch (m) {
+      case 1: MOEX_DN(1); break;
+      case 2: MOEX_DN(2); break;
+      case 3: MOEX_DN(3); break;
+      case 4: MOEX_DN(4); break;
+      case 5: MOEX_DN(5); break;
+      case 6: MOEX_DN(6); break;
+      case 7: MOEX_DN(7); break;
+      default: MOEX_DN(8); break;
+    }
+#undef MOEX_DN
+  }
+  named_bar_sync(1, nthr);
+  // combine: out[t][r] = sum over slots in order of w[t,slot] * o[(t,slot)][r]
+  for (int i = threadIdx.x; i < a.T * nrows; i += nthr) {
+    const int t = i / nrows, rl = i % nrows;
+    float acc = 0.f;
+    for (int s = 0; s < a.k; ++s) {
+      const int j = t * a.k + s;
+      const int e = a.ids[j];
+      if (e < 0 || e >= a.E) continue;
+      acc = __fadd_rn(acc, __fmul_rn(a.w[j], osum[j * rows_max + rl]));
+    }
+    a.out[static_cast<int64_t>(t) * a.H + row_begin + rl] = acc;
+  }
+}
+
+// ============================================================== host side
+
+size_t moe_decode_ws_bytes(int T, int k, int64_t hidden, int64_t inter) {
+  (void)hidden;
+  const size_t n = static_cast<size_t>(T) * k;
+  const size_t hq = (n * inter + 255) / 256 * 256;
+  return hq + n * (inter / QK) * 8;
+}
+
+namespace {
+
+template <int WPS>
+moex_status launch_gu(const DecodeArgs& base, int smem_cap, cudaStream_t s) {
+  DecodeArgs a = base;
+  const int NB = a.H / QK, NS = num_slices(NB);
+  a.stage_bytes = ((SR * (a.gu_qrow + a.gu_scrow)) + 127) & ~127;
+  int nst = 16;
+  for (; nst >= 2; --nst)
+    if (GuSmem(a.T, a.H, NS, nst, a.stage_bytes).total <= smem_cap) break;
+  if (nst < 2) return MOEX_EUNSUPPORTED;
+  a.nst = nst;
+  const GuSmem L(a.T, a.H, NS, nst, a.stage_bytes);
+  auto kern = moe_gu_kernel<WPS>;
+  if (ensure_smem(reinterpret_cast<const void*>(kern), L.total) != cudaSuccess) return MOEX_ECUDA;
+  // grid: enough CTAs for the largest possible unit count is not known on
+  // the host (it depends on the routing); use every SM.
+  const int grid = sm_count();
+  const int threads = (NS * WPS + 1) * 32;
+  return cuda_status(launch_pdl(kern, dim3(grid), dim3(threads), L.total, s, a));
+}
+
+template <int FMT, int WPS>
+moex_status launch_dn(const DecodeArgs& base, int smem_cap, cudaStream_t s) {
+  DecodeArgs a = base;
+  const int NB = a.I / QK, NS = num_slices(NB);
+  a.stage_bytes = ((SR * (a.dn_qrow + a.dn_scrow)) + 127) & ~127;
+  const int grid = a.H < sm_count() ? a.H : sm_count();
+  const int rows_max = (a.H + grid - 1) / grid;
+  int nst = 16;
+  for (; nst >= 2; --nst)
+    if (DnSmem(a.n, a.I, NS, rows_max, nst, a.stage_bytes).total <= smem_cap) break;
+  if (nst < 2) return MOEX_EUNSUPPORTED;
+  a.nst = nst;
+  const DnSmem L(a.n, a.I, NS, rows_max, nst, a.stage_bytes);
+  auto kern = moe_dn_kernel<FMT, WPS>;
+  if (ensure_smem(reinterpret_cast<const void*>(kern), L.total) != cudaSuccess) return MOEX_ECUDA;
+  const int threads = (NS * WPS + 1) * 32;
+  return cuda_status(launch_pdl(kern, dim3(grid), dim3(threads), L.total, s, a));
+}
+
+template <int FMT>
+moex_status launch_dn_fmt(const DecodeArgs& a, int cap, cudaStream_t s) {
+  switch (warps_per_slice(num_slices(a.I / QK))) {
+    case 4: return launch_dn<FMT, 4>(a, cap, s);
+    case 2: return launch_dn<FMT, 2>(a, cap, s);
+    default: return launch_dn<FMT, 1>(a, cap, s);
+  }
+}
+
+}  // namespace
+
+moex_status launch_moe_decode(const moex_qweight* gu, const moex_qweight* dn, const float* x, int T,
+                              const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,
+                              float* gu_dbg, float* h_dbg, int8_t* hq_dbg, float* hds_dbg, cudaStream_t s) {
+  (void)ws_bytes;
+  DecodeArgs a = {};
+  a.H = static_cast<int>(gu->K);
+  a.I = static_cast<int>(gu->rows / 2);
+  a.E = gu->n_mats;
+  a.T = T;
+  a.k = k;
+  a.n = T * k;
+  a.gu_qs = static_cast<const uint8_t*>(gu->qs);
+  a.gu_sc = static_cast<const uint8_t*>(gu->scales);
+  a.gu_qrow = static_cast<int>(qs_row_bytes(gu->fmt, gu->K));
+  a.gu_scrow = static_cast<int>(sc_row_bytes(gu->K));
+  a.dn_qs = static_cast<const uint8_t*>(dn->qs);
+  a.dn_sc = static_cast<const uint8_t*>(dn->scales);
+  a.dn_qrow = static_cast<int>(qs_row_bytes(dn->fmt, dn->K));
+  a.dn_scrow = static_cast<int>(sc_row_bytes(dn->K));
+  a.x = x;
+  a.ids = ids;
+  a.w = w;
+  a.out = out;
+  a.hq = static_cast<int8_t*>(ws);
+  a.hds = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + (static_cast<size_t>(a.n) * a.I + 255) / 256 * 256);
+  a.gu_dbg = gu_dbg;
+  a.h_dbg = h_dbg;
+  a.hq_dbg = hq_dbg;
+  a.hds_dbg = hds_dbg;
+  a.status = device_status_ptr();
+  const int cap = max_smem_optin();
+  const int NSg = num_slices(a.H / QK), NSd = num_slices(a.I / QK);
+  if (NSg * warps_per_slice(NSg) > 15 || NSd * warps_per_slice(NSd) > 15) return MOEX_EUNSUPPORTED;
+  moex_status st;
+  switch (warps_per_slice(NSg)) {
+    case 4: st = launch_gu<4>(a, cap, s); break;
+    case 2: st = launch_gu<2>(a, cap, s); break;
+    default: st = launch_gu<1>(a, cap, s); break;
+  }
+  if (st != MOEX_OK) return st;
+  return dn->fmt == MOEX_Q8_0 ? launch_dn_fmt<MOEX_Q8_0>(a, cap, s) : launch_dn_fmt<MOEX_IQ4_NL>(a, cap, s);
+}
+
+}  // namespace moex

@@ -1,0 +1,103 @@
+"""The C-ABI library loads, exports every symbol include/moex.h declares, and
+rejects bad arguments on the host before touching the GPU (CPU-only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from helpers import ROOT, ensure_lib
+
+HEADER = os.path.join(ROOT, "include", "moex.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moex_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["moex_quantize_q8_1", "moex_qgemv", "moex_moe_decode", "moex_weight_pack", "moex_route_topk",
+              "moex_device_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = ensure_lib()
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol():
+    import moe_expert_gb300 as mx
+    assert set(declared_functions()) <= set(mx.SIGNATURES)
+
+
+def test_status_strings_and_version():
+    L = ensure_lib()
+    assert L.moex_version() == 1
+    assert L.moex_status_string(0) == b"ok"
+    assert L.moex_status_string(7) == b"workspace too small"
+
+
+def test_plane_bytes():
+    import moe_expert_gb300 as mx
+    L = ensure_lib()
+    q, s = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.moex_weight_plane_bytes(1, 1, 8192, 2560, ctypes.byref(q), ctypes.byref(s)) == 0
+    assert (q.value, s.value) == (8192 * 2560, 8192 * 160)
+    assert L.moex_weight_plane_bytes(2, 128, 2560, 1536, ctypes.byref(q), ctypes.byref(s)) == 0
+    assert (q.value, s.value) == (128 * 2560 * 768, 128 * 2560 * 96)
+    # K = 96: 3 scales = 6 bytes, padded to 16
+    assert L.moex_weight_plane_bytes(1, 1, 4, 96, ctypes.byref(q), ctypes.byref(s)) == 0
+    assert s.value == 4 * 16
+    assert L.moex_weight_plane_bytes(1, 1, 4, 100, ctypes.byref(q), ctypes.byref(s)) == 1   # K % 32
+    assert L.moex_weight_plane_bytes(9, 1, 4, 96, ctypes.byref(q), ctypes.byref(s)) == 3    # bad fmt
+
+
+def test_host_validation_rejects_before_launch():
+    import moe_expert_gb300 as mx
+    L = ensure_lib()
+    null = ctypes.c_void_p(0)
+    buf = ctypes.create_string_buffer(4096 + 16)
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    p = ctypes.c_void_p(base)
+    # null pointers
+    assert L.moex_quantize_q8_1(null, 64, 1, 64, p, p, null) == 1
+    assert L.moex_qgemv(None, p, p, 1, p, 8, null) == 1
+    # K not a multiple of 32, ncols out of range
+    assert L.moex_quantize_q8_1(p, 48, 1, 48, p, p, null) == 1
+    assert L.moex_quantize_q8_1(p, 64, 0, 64, p, p, null) == 1
+    assert L.moex_quantize_q8_1(p, 64, 65, 64, p, p, null) == 1
+    # misaligned activation pointer
+    assert L.moex_quantize_q8_1(ctypes.c_void_p(base + 4), 64, 1, 64, p, p, null) == 2
+    w = mx.QWeight(1, 1, 8, 64, base, base)
+    assert L.moex_qgemv(ctypes.byref(w), p, p, 1, p, 4, null) == 1          # ldy < rows
+    w_bad = mx.QWeight(1, 1, 8, 64, base + 8, base)
+    assert L.moex_qgemv(ctypes.byref(w_bad), p, p, 1, p, 8, null) == 2      # misaligned plane
+    w_fmt = mx.QWeight(5, 1, 8, 64, base, base)
+    assert L.moex_qgemv(ctypes.byref(w_fmt), p, p, 1, p, 8, null) == 3
+    # routing
+    assert L.moex_route_topk(p, 4, 8, 9, p, p, null) == 1                   # k > E
+    assert L.moex_route_topk(p, 4, 2048, 8, p, p, null) == 1                # E too large
+
+
+def test_decode_validation_and_workspace():
+    import moe_expert_gb300 as mx
+    L = ensure_lib()
+    null = ctypes.c_void_p(0)
+    buf = ctypes.create_string_buffer(4096 + 16)
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    p = ctypes.c_void_p(base)
+    need = L.moex_moe_decode_workspace_bytes(3, 8, 2560, 1536)
+    assert need >= 24 * 1536 + 24 * 48 * 8
+    gu = mx.QWeight(1, 128, 3072, 2560, base, base)
+    dn = mx.QWeight(2, 128, 2560, 1536, base, base)
+    assert L.moex_moe_decode(ctypes.byref(gu), ctypes.byref(dn), p, 3, p, p, 8, p, p, need - 1, null) == 7
+    assert L.moex_moe_decode(ctypes.byref(gu), ctypes.byref(dn), p, 9, p, p, 8, p, p, 1 << 30, null) == 1
+    dn_bad = mx.QWeight(2, 128, 2560, 1024, base, base)                    # inter mismatch
+    assert L.moex_moe_decode(ctypes.byref(gu), ctypes.byref(dn_bad), p, 3, p, p, 8, p, p, 1 << 30, null) == 1
+    gu_iq = mx.QWeight(2, 128, 3072, 2560, base, base)                     # gate/up must be Q8_0
+    assert L.moex_moe_decode(ctypes.byref(gu_iq), ctypes.byref(dn), p, 3, p, p, 8, p, p, 1 << 30, null) == 3
