@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <unordered_map>
 
 #include "common.cuh"
 #include "gemv_core.cuh"
@@ -61,9 +62,19 @@ int max_smem_optin() {
 }
 
 cudaError_t ensure_smem(const void* func, size_t bytes) {
-  // Cheap enough to set on every call for the few kernel instances used;
-  // the attribute is per function and device.
-  return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  // The attribute is per function and device; it is raised once to the
+  // largest size seen, so calls captured into a CUDA graph after a first
+  // (warm-up) call make no attribute call at all.
+  static std::mutex mu;
+  static std::unordered_map<const void*, size_t> seen[MAX_DEV];
+  const int d = current_device();
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = seen[d].find(func);
+  if (it != seen[d].end() && it->second >= bytes) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) seen[d][func] = bytes;
+  return e;
 }
 
 }  // namespace moex

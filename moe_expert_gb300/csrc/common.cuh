@@ -45,6 +45,30 @@ __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }
 
+// ----------------------------------------------------------------- tracing
+
+// Timeline hooks: compiled to nothing unless MOEX_TRACE is defined (a
+// profiling build, which defines moex::g_moex_trace and g_moex_trace_ord
+// before including the kernels, records %globaltimer at fixed points of
+// each CTA).
+#ifdef MOEX_TRACE
+#define MOEX_TRACE_BEGIN()                                                         \
+  __shared__ unsigned int moex_trace_ord;                                          \
+  if (threadIdx.x == 0) moex_trace_ord = atomicAdd(&g_moex_trace_ord[blockIdx.x & 4095], 1u)
+#define MOEX_TRACE_STAMP(k)                                                        \
+  do {                                                                             \
+    if (threadIdx.x == 0 && g_moex_trace && moex_trace_ord < 64)                   \
+      g_moex_trace[((size_t)moex_trace_ord * 4096 + (blockIdx.x & 4095)) * 8 + (k)] = moex::global_timer_ns(); \
+  } while (0)
+#else
+#define MOEX_TRACE_BEGIN() \
+  do {                     \
+  } while (0)
+#define MOEX_TRACE_STAMP(k) \
+  do {                      \
+  } while (0)
+#endif
+
 // ----------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -10,16 +10,18 @@
 // split of #242).
 //
 // GB300 layout (not the pages' warp-per-row kernels):
-//  * a single producer thread streams contiguous row ranges of the weight
-//    planes into a ring of shared-memory stages with cp.async.bulk (16-byte
-//    aligned bulk copies completing on mbarriers), so each SM keeps tens of
-//    KB of HBM reads in flight from the first cycle;
-//  * the K axis is cut into slices of 16 blocks; a consumer warp owns one
-//    slice and its 16 lanes x 2 halves hold one 32-value block each, with the
+//  * the K axis is cut into slices of 16 blocks; a warp owns one slice and
+//    its 16 lanes x 2 halves hold one 32-value block each, with the
 //    activations of that block for all columns in registers (loaded once per
 //    column set), so activations cost no shared-memory traffic per row;
-//  * a stage of 8 rows is shared by all consumer warps (every slice, every
-//    row), so the last stage to arrive is finished quickly;
+//  * every lane streams exactly the weight bytes it will consume (its block
+//    of each of its rows) with 16-byte cp.async copies into its own slots of
+//    a shared-memory ring, several 8-row stages ahead: tens of KB per SM stay
+//    in flight without holding registers, a warp's copies cover contiguous
+//    512-byte row pieces, and no producer warp, mbarrier or cross-warp
+//    handshake is needed for the weights;
+//  * a stage of 8 rows is shared by all warps (every slice, every row), so
+//    the last stage to arrive is finished quickly;
 //  * per-lane partial sums are reduced over the 16 lanes with a recursive
 //    halving exchange (xor 8, 4, 2, 1) whose summation tree does not depend
 //    on the number of columns, then over the slices in slice order, so a
@@ -35,6 +37,7 @@ namespace moex {
 
 constexpr int SR = 8;        // rows per pipeline stage
 constexpr int SLICE = 16;    // blocks per K slice (one per lane of a half warp)
+constexpr int NRED = 4;      // slots of the cross-slice reduction buffer
 
 __host__ __device__ inline int64_t qs_row_bytes(int fmt, int64_t K) { return fmt == MOEX_Q8_0 ? K : K / 2; }
 __host__ __device__ inline int64_t sc_row_bytes(int64_t K) { return ((K / QK) * 2 + 15) / 16 * 16; }
@@ -53,10 +56,7 @@ struct FmtTraits<MOEX_IQ4_NL> {
 // ----------------------------------------------------------------- activations
 
 // Per-lane activation registers for one block b and C columns.
-//  Q8_0 lanes read their weight block as two 16-byte halves in the order
-//  h0 = (li >> 2) & 1, then 1 - h0 (this spreads the 8 lanes of a shared
-//  memory phase over all 32 banks); the activation words are held in the
-//  same order.
+//  Q8_0: the 8 words in natural order.
 //  IQ4_NL weights decode to the byte order x[j], x[j+16], x[j+1], x[j+17]
 //  (low and high nibble of consecutive index bytes); the activation words
 //  are held permuted to match:
@@ -69,11 +69,12 @@ struct ActRegs {
 };
 
 // Loads activations of block b (natural order: column c's quants at
-// xcol[c], its scales at dcol[c]; dcol == nullptr gives unit scales) into
-// registers.  Invalid blocks get zeros.
+// xcol[c], its d scales at dcol[c][b * dstride]; dcol == nullptr gives unit
+// scales) into registers.  Invalid blocks get zeros.  The pointers may be
+// shared or global memory.
 template <int FMT, int C>
 __device__ __forceinline__ void load_act(ActRegs<FMT, C>& r, const int8_t* const* xcol, const float* const* dcol,
-                                         int b, bool valid, int li) {
+                                         int b, bool valid, int li, int dstride = 1) {
 #pragma unroll
   for (int c = 0; c < C; ++c) {
     if (!valid) {
@@ -86,11 +87,8 @@ __device__ __forceinline__ void load_act(ActRegs<FMT, C>& r, const int8_t* const
     uint4 lo = *reinterpret_cast<const uint4*>(src);
     uint4 hi = *reinterpret_cast<const uint4*>(src + 16);
     if constexpr (FMT == MOEX_Q8_0) {
-      const bool swap = (li >> 2) & 1;
-      const uint4 f = swap ? hi : lo;
-      const uint4 s = swap ? lo : hi;
-      r.a[c][0] = f.x; r.a[c][1] = f.y; r.a[c][2] = f.z; r.a[c][3] = f.w;
-      r.a[c][4] = s.x; r.a[c][5] = s.y; r.a[c][6] = s.z; r.a[c][7] = s.w;
+      r.a[c][0] = lo.x; r.a[c][1] = lo.y; r.a[c][2] = lo.z; r.a[c][3] = lo.w;
+      r.a[c][4] = hi.x; r.a[c][5] = hi.y; r.a[c][6] = hi.z; r.a[c][7] = hi.w;
     } else {
       const uint32_t X[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
@@ -99,27 +97,25 @@ __device__ __forceinline__ void load_act(ActRegs<FMT, C>& r, const int8_t* const
         r.a[c][2 * i + 1] = prmt(X[i], X[i + 4], 0x7362);
       }
     }
-    r.d[c] = dcol ? dcol[c][b] : 1.f;
+    r.d[c] = dcol ? dcol[c][b * dstride] : 1.f;
   }
 }
 
 // ----------------------------------------------------------------- one row
 
-// Integer dots of one weight block (row pointer at the block) with C columns,
-// then p[c] = I * (dw * dx[c]) in FP32.
+// Integer dots of one weight block with C columns, then
+// p[c] = I * (dw * dx[c]) in FP32.  The block's quant bytes are given as
+// 16-byte chunks q0 (and q1 for Q8_0).
 template <int FMT, int C>
-__device__ __forceinline__ void block_row_dots(const uint8_t* wq, float dw, const ActRegs<FMT, C>& act, int li,
-                                               float* p, int* I_out = nullptr) {
+__device__ __forceinline__ void block_dots_from(uint4 q0, uint4 q1, float dw, const ActRegs<FMT, C>& act, float* p,
+                                                int* I_out = nullptr) {
   uint32_t wv[8];
   if constexpr (FMT == MOEX_Q8_0) {
-    const int h0 = (li >> 2) & 1;
-    const uint4 f = *reinterpret_cast<const uint4*>(wq + 16 * h0);
-    const uint4 s = *reinterpret_cast<const uint4*>(wq + 16 * (1 - h0));
-    wv[0] = f.x; wv[1] = f.y; wv[2] = f.z; wv[3] = f.w;
-    wv[4] = s.x; wv[5] = s.y; wv[6] = s.z; wv[7] = s.w;
+    wv[0] = q0.x; wv[1] = q0.y; wv[2] = q0.z; wv[3] = q0.w;
+    wv[4] = q1.x; wv[5] = q1.y; wv[6] = q1.z; wv[7] = q1.w;
   } else {
-    const uint4 n = *reinterpret_cast<const uint4*>(wq);
-    const uint32_t W[4] = {n.x, n.y, n.z, n.w};
+    (void)q1;
+    const uint32_t W[4] = {q0.x, q0.y, q0.z, q0.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t fl = W[i] ^ 0x88888888u;
@@ -135,6 +131,15 @@ __device__ __forceinline__ void block_row_dots(const uint8_t* wq, float dw, cons
     if (I_out) I_out[c] = I;
     p[c] = __fmul_rn(__int2float_rn(I), __fmul_rn(dw, act.d[c]));
   }
+}
+
+// Same, reading the block from memory at wq.
+template <int FMT, int C>
+__device__ __forceinline__ void block_row_dots(const uint8_t* wq, float dw, const ActRegs<FMT, C>& act, float* p,
+                                               int* I_out = nullptr) {
+  const uint4 q0 = *reinterpret_cast<const uint4*>(wq);
+  const uint4 q1 = FMT == MOEX_Q8_0 ? *reinterpret_cast<const uint4*>(wq + 16) : q0;
+  block_dots_from<FMT, C>(q0, q1, dw, act, p, I_out);
 }
 
 // ----------------------------------------------------------------- reduction
@@ -165,50 +170,152 @@ __device__ __forceinline__ void halving_reduce(float* v, int lane) {
 
 __host__ __device__ constexpr int pow2_ceil(int v) { return v <= 1 ? 1 : 2 * pow2_ceil((v + 1) / 2); }
 
-// ----------------------------------------------------------------- consumer layout
+// ----------------------------------------------------------------- lane ring
 
-// Consumer warp w owns slice ks = w / WPS; its half `hf` (lane >> 4) and
-// index jw = w % WPS give the stage rows jw*2 + hf + 2*WPS*i, i < RPH, with
+// Warp w owns slice ks = w / WPS; its half `hf` (lane >> 4) and index
+// jw = w % WPS give the stage rows jw*2 + hf + 2*WPS*i, i < RPH, with
 // RPH = SR / (2*WPS).
 struct ConsumerPos {
-  int ks, jw, hf, li, lane;
+  int ks, jw, hf, li, lane, warp;
 };
 
-// Computes one stage for one consumer warp and writes its per-slice partial
-// sums red[row][ks][c] (row < nrows).  wq_stage / sc_stage are the stage's
-// quant rows (stride qrow bytes) and FP16 scale rows (stride scrow bytes).
-template <int FMT, int C, int WPS>
-__device__ __forceinline__ void stage_partials(const uint8_t* wq_stage, const uint8_t* sc_stage, int qrow, int scrow,
-                                               int nrows, int NB, int NS, const ConsumerPos& pos,
-                                               const ActRegs<FMT, C>& act, float* red) {
-  constexpr int RPH = SR / (2 * WPS);
-  constexpr int V = RPH * C;
-  constexpr int N = pow2_ceil(V);
-  float v[N];
+__device__ __forceinline__ ConsumerPos consumer_pos(int warp, int lane, int WPS) {
+  ConsumerPos p;
+  p.warp = warp;
+  p.ks = warp / WPS;
+  p.jw = warp % WPS;
+  p.lane = lane;
+  p.hf = lane >> 4;
+  p.li = lane & 15;
+  return p;
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most n of this thread's most recent cp.async groups are pending.
+__device__ __forceinline__ void cp_async_wait(int n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    case 7: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 8;" ::: "memory"); break;
+  }
+}
+
+// Geometry of the per-lane ring.  One ring slot holds one 8-row stage:
+//   quants: [rr][chunk][warp][lane] x 16 bytes  (a warp's accesses for one
+//           (rr, chunk) are 512 contiguous bytes: no bank conflicts)
+//   scales: [rr][warp][lane] x 4 bytes (the FP16 scale word holding the
+//           lane's block; block b is its half b & 1)
+template <int FMT, int WPS>
+struct Ring {
+  static constexpr int RPH = SR / (2 * WPS);
+  static constexpr int QB = FmtTraits<FMT>::QBYTES;
+  static constexpr int NCH = QB / 16;
+  __host__ __device__ static int slot_bytes(int nwc) { return nwc * 32 * RPH * (NCH * 16 + 4); }
+  __device__ static uint8_t* qptr(uint8_t* slot, int nwc, int rr, int h, int warp, int lane) {
+    return slot + ((((rr * NCH + h) * nwc + warp) * 32 + lane) * 16);
+  }
+  __device__ static uint8_t* sptr(uint8_t* slot, int nwc, int rr, int warp, int lane) {
+    return slot + nwc * 32 * RPH * NCH * 16 + (((rr * nwc + warp) * 32 + lane) * 4);
+  }
+};
+
+// Issues this lane's copies of one stage into `slot`: rows [0, nrows) of the
+// stage start at qsrc / ssrc (plane row strides qrow / scrow).  The caller
+// commits the group.
+template <int FMT, int WPS>
+__device__ __forceinline__ void ring_issue(uint8_t* slot, int nwc, const ConsumerPos& p, const uint8_t* qsrc,
+                                           const uint8_t* ssrc, int nrows, int qrow, int scrow, int NB) {
+  using R = Ring<FMT, WPS>;
+  const int b = p.ks * SLICE + p.li;
+  if (b >= NB) return;
 #pragma unroll
-  for (int i = 0; i < N; ++i) v[i] = 0.f;
-  const int b = pos.ks * SLICE + pos.li;
-  const bool bvalid = b < NB;
+  for (int rr = 0; rr < R::RPH; ++rr) {
+    const int row = p.jw * 2 + p.hf + 2 * WPS * rr;
+    if (row < nrows) {
+      const uint8_t* q = qsrc + static_cast<int64_t>(row) * qrow + b * R::QB;
 #pragma unroll
-  for (int rr = 0; rr < RPH; ++rr) {
-    const int row = pos.jw * 2 + pos.hf + 2 * WPS * rr;
-    if (bvalid && row < nrows) {
-      const uint8_t* wq = wq_stage + row * qrow + b * FmtTraits<FMT>::QBYTES;
-      const float dw = __half2float(reinterpret_cast<const __half*>(sc_stage + row * scrow)[b]);
-      block_row_dots<FMT, C>(wq, dw, act, pos.li, &v[rr * C]);
+      for (int h = 0; h < R::NCH; ++h) cp_async16(R::qptr(slot, nwc, rr, h, p.warp, p.lane), q + 16 * h);
+      cp_async4(R::sptr(slot, nwc, rr, p.warp, p.lane), ssrc + static_cast<int64_t>(row) * scrow + 4 * (b >> 1));
     }
   }
-  halving_reduce<N, 8>(v, pos.lane);
-  // scatter to red[row][ks][c]
-  const int li = pos.li;
+}
+
+// Asks L2 for the 128-byte lines of this lane's part of one stage (one lane
+// in four: a line holds the pieces of four neighbouring lanes).
+template <int FMT, int WPS>
+__device__ __forceinline__ void lane_prefetch_l2(const ConsumerPos& p, const uint8_t* qsrc, const uint8_t* ssrc,
+                                                 int nrows, int qrow, int scrow, int NB) {
+  using R = Ring<FMT, WPS>;
+  const int b = p.ks * SLICE + p.li;
+  if (b >= NB || (p.li & 3) != 0) return;
+#pragma unroll
+  for (int rr = 0; rr < R::RPH; ++rr) {
+    const int row = p.jw * 2 + p.hf + 2 * WPS * rr;
+    if (row < nrows) {
+      const uint8_t* q = qsrc + static_cast<int64_t>(row) * qrow + b * R::QB;
+#pragma unroll
+      for (int h = 0; h < R::NCH * 4; h += 8)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(q + 16 * h) : "memory");
+      if ((p.li & 15) == 0)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(ssrc + static_cast<int64_t>(row) * scrow + 4 * (b >> 1))
+                     : "memory");
+    }
+  }
+}
+
+// Per-lane partial sums of one stage from the ring: v[rr*C + c] for this
+// lane's rows (zero for rows >= nrows or blocks >= NB).
+template <int FMT, int C, int WPS, int N>
+__device__ __forceinline__ void ring_partials(uint8_t* slot, int nwc, const ConsumerPos& p, int nrows, int NB,
+                                              const ActRegs<FMT, C>& act, float (&v)[N]) {
+  using R = Ring<FMT, WPS>;
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = 0.f;
+  const int b = p.ks * SLICE + p.li;
+  if (b >= NB) return;
+#pragma unroll
+  for (int rr = 0; rr < R::RPH; ++rr) {
+    const int row = p.jw * 2 + p.hf + 2 * WPS * rr;
+    if (row < nrows) {
+      const uint4 q0 = *reinterpret_cast<const uint4*>(R::qptr(slot, nwc, rr, 0, p.warp, p.lane));
+      const uint4 q1 = R::NCH > 1 ? *reinterpret_cast<const uint4*>(R::qptr(slot, nwc, rr, R::NCH - 1, p.warp, p.lane))
+                                  : q0;
+      const uint32_t sw = *reinterpret_cast<const uint32_t*>(R::sptr(slot, nwc, rr, p.warp, p.lane));
+      const uint16_t hb = static_cast<uint16_t>((b & 1) ? (sw >> 16) : (sw & 0xFFFFu));
+      const float dw = __half2float(__ushort_as_half(hb));
+      block_dots_from<FMT, C>(q0, q1, dw, act, &v[rr * C]);
+    }
+  }
+}
+
+// Reduces a lane's partials over its half warp and writes them to
+// red[row][ks][c] (row < nrows).
+template <int C, int WPS, int N>
+__device__ __forceinline__ void reduce_to_red(float (&v)[N], const ConsumerPos& p, int nrows, int NS, float* red) {
+  constexpr int RPH = SR / (2 * WPS);
+  constexpr int V = RPH * C;
+  halving_reduce<N, 8>(v, p.lane);
+  const int li = p.li;
   if constexpr (N >= 16) {
 #pragma unroll
     for (int i = 0; i < N / 16; ++i) {
       const int idx = li * (N / 16) + i;
       if (idx < V) {
         const int rr = idx / C, c = idx % C;
-        const int row = pos.jw * 2 + pos.hf + 2 * WPS * rr;
-        if (row < nrows) red[(row * NS + pos.ks) * C + c] = v[i];
+        const int row = p.jw * 2 + p.hf + 2 * WPS * rr;
+        if (row < nrows) red[(row * NS + p.ks) * C + c] = v[i];
       }
     }
   } else {
@@ -217,9 +324,28 @@ __device__ __forceinline__ void stage_partials(const uint8_t* wq_stage, const ui
       const int idx = li / REP;
       if (idx < V) {
         const int rr = idx / C, c = idx % C;
-        const int row = pos.jw * 2 + pos.hf + 2 * WPS * rr;
-        if (row < nrows) red[(row * NS + pos.ks) * C + c] = v[0];
+        const int row = p.jw * 2 + p.hf + 2 * WPS * rr;
+        if (row < nrows) red[(row * NS + p.ks) * C + c] = v[0];
       }
+    }
+  }
+}
+
+template <int C, int WPS>
+struct Vals {
+  static constexpr int N = pow2_ceil((SR / (2 * WPS)) * C);
+};
+
+// Waits (bounded) until the red slot is free for stage `it`: its previous
+// user (stage it - nred) has been summed.  Returns false on timeout / abort.
+__device__ __forceinline__ bool red_slot_wait(volatile int* seq, int it, volatile int* abort) {
+  if (*seq == it) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (*seq == it) return true;
+    if ((i & 63u) == 0) {
+      if (abort && *abort) return false;
+      if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
     }
   }
 }
@@ -254,5 +380,19 @@ __device__ __forceinline__ bool stage_arrive_last(int* cnt, int nwarps, int lane
 // Consumer warp count for a K with NB blocks, and warps per slice.
 __host__ __device__ inline int num_slices(int NB) { return (NB + SLICE - 1) / SLICE; }
 __host__ __device__ inline int warps_per_slice(int NS) { return NS <= 3 ? 4 : (NS <= 7 ? 2 : 1); }
+
+// ----------------------------------------------------------------- L2 prefetch
+
+// Asks the TMA unit to bring [src, src+bytes) into L2 (no shared memory, no
+// completion); src and bytes multiples of 16.  Issued in pieces of <= 64 KB.
+__device__ __forceinline__ void prefetch_l2(const void* src, int64_t bytes) {
+  const uint8_t* p = static_cast<const uint8_t*>(src);
+  while (bytes > 0) {
+    const uint32_t n = static_cast<uint32_t>(bytes < 65536 ? bytes : 65536);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
+    p += n;
+    bytes -= n;
+  }
+}
 
 }  // namespace moex

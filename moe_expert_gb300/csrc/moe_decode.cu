@@ -25,7 +25,6 @@
 namespace moex {
 
 constexpr int MAX_ENTRIES = 64;   // T * k
-constexpr int MAX_TOKENS = 8;
 constexpr int MAX_GROUP = 8;      // entries per pass of one expert
 
 struct DecodeArgs {
@@ -96,16 +95,18 @@ __device__ void build_groups(Groups& G, const int32_t* ids, int n, int E, uint32
 
 // ============================================================== gate / up
 
+
+constexpr int NUB = 3;    // unit buffers (SwiGLU inputs of one unit)
+
 struct GuSmem {
-  int bars, cnt, ucnt, abort_flag, groups, xs, xd, red, ubuf, stages, total;
-  int nub;
-  __host__ __device__ GuSmem(int T, int H, int NS, int nst, int stage_bytes) {
-    nub = nst / 8 + 2;
+  int cnt, seq, useq, ucnt, abort_flag, groups, xs, xd, red, ubuf, ring, total;
+  __host__ __device__ GuSmem(int T, int H, int NS, int nst, int slot_bytes) {
     const int NB = H / QK;
     int o = 0;
-    bars = o; o += 16 * nst;
-    cnt = o; o += 4 * nst;
-    ucnt = o; o += 4 * nub;
+    cnt = o; o += 4 * NRED;
+    seq = o; o += 4 * NRED;
+    useq = o; o += 4 * NUB;
+    ucnt = o; o += 4 * NUB;
     abort_flag = o; o += 16;
     o = (o + 15) & ~15;
     groups = o; o += static_cast<int>(sizeof(Groups));
@@ -114,10 +115,10 @@ struct GuSmem {
     o = (o + 15) & ~15;
     xd = o; o += 4 * T * NB;
     o = (o + 15) & ~15;
-    red = o; o += 4 * nst * SR * NS * MAX_GROUP;
-    ubuf = o; o += 4 * nub * 64 * MAX_GROUP;
+    red = o; o += 4 * NRED * SR * NS * MAX_GROUP;
+    ubuf = o; o += 4 * NUB * 64 * MAX_GROUP;
     o = (o + 127) & ~127;
-    stages = o; o += nst * stage_bytes;
+    ring = o; o += nst * slot_bytes;
     total = o;
   }
 };
@@ -160,12 +161,23 @@ __device__ __forceinline__ void gu_epilogue(const DecodeArgs& a, const Groups& G
   }
 }
 
-// One work unit (group g, intermediate block ib): 8 stages of 8 rows.
-template <int C, int WPS>
-__device__ __forceinline__ void gu_unit(const DecodeArgs& a, const Groups& G, int g, int ib, int ui, int NB, int NS,
-                                        int nwc, const ConsumerPos& pos, const int8_t* xs, const float* xd,
-                                        uint64_t* full, uint64_t* empty, int* cnt, int* ucnt, float* red, float* ubuf,
-                                        int nub, const uint8_t* stages, volatile int* abort_flag, bool& dead) {
+// Shared state of one decode CTA's stage loop.
+struct StageCtx {
+  uint8_t* ring;
+  int slot_bytes, nst, nwc, NS, NB;
+  int* cnt;
+  volatile int* seq;
+  volatile int* abort_flag;
+  float* red;
+  uint32_t* status;
+};
+
+// One work unit (group g, intermediate block ib): 8 stages of 8 rows; stage
+// indices it0 .. it0+7.  `issue(it)` refills the ring for any later stage.
+template <int C, int WPS, typename Issue>
+__device__ __forceinline__ void gu_unit(const DecodeArgs& a, const Groups& G, int g, int ib, int ui, int it0,
+                                        const StageCtx& S, const ConsumerPos& pos, const int8_t* xs, const float* xd,
+                                        int* ucnt, volatile int* useq, float* ubuf, bool& dead, Issue&& issue) {
   ActRegs<MOEX_Q8_0, C> act;
   {
     const int8_t* xcol[C];
@@ -174,79 +186,98 @@ __device__ __forceinline__ void gu_unit(const DecodeArgs& a, const Groups& G, in
     for (int c = 0; c < C; ++c) {
       const int t = G.ent[G.gstart[g] + c] / a.k;
       xcol[c] = xs + t * a.H;
-      dcol[c] = xd + t * NB;
+      dcol[c] = xd + t * S.NB;
     }
     const int b = pos.ks * SLICE + pos.li;
-    load_act<MOEX_Q8_0, C>(act, xcol, dcol, b, b < NB, pos.li);
+    load_act<MOEX_Q8_0, C>(act, xcol, dcol, b, b < S.NB, pos.li);
   }
-  float* ub = ubuf + (ui % nub) * 64 * MAX_GROUP;
+  constexpr int N = Vals<C, WPS>::N;
+  float* ub = ubuf + (ui % NUB) * 64 * MAX_GROUP;
   for (int s = 0; s < 8; ++s) {
-    const int it = ui * 8 + s;
-    const int slot = it % a.nst;
-    if (!dead && !mbar_wait(&full[slot], (it / a.nst) & 1, abort_flag)) {
+    const int it = it0 + s;
+    cp_async_wait(S.nst - 1);
+    float v[N];
+    if (!dead) ring_partials<MOEX_Q8_0, C, WPS, N>(S.ring + static_cast<size_t>(it % S.nst) * S.slot_bytes, S.nwc, pos,
+                                                   SR, S.NB, act, v);
+    issue(it + S.nst);
+    if (dead) continue;
+    const int rs_slot = it % NRED;
+    if (!red_slot_wait(&S.seq[rs_slot], it, S.abort_flag) || (s == 0 && !red_slot_wait(&useq[ui % NUB], ui, S.abort_flag))) {
       if (pos.lane == 0) {
-        *abort_flag = 1;
-        flag_status(a.status, DEV_TIMEOUT_PIPE);
+        *S.abort_flag = 1;
+        flag_status(S.status, DEV_TIMEOUT_PIPE);
       }
       dead = true;
+      continue;
     }
-    if (dead) continue;
-    const uint8_t* stage = stages + static_cast<size_t>(slot) * a.stage_bytes;
-    float* rs = red + slot * (SR * NS * MAX_GROUP);
-    stage_partials<MOEX_Q8_0, C, WPS>(stage, stage + SR * a.gu_qrow, a.gu_qrow, a.gu_scrow, SR, NB, NS, pos, act,
-                                      rs);
-    if (stage_arrive_last(&cnt[slot], nwc, pos.lane)) {
-      stage_final<C>(rs, SR, NS, pos.lane,
-                     [&](int row, int c, float v) { ub[(s * SR + row) * MAX_GROUP + c] = v; });
-      if (pos.lane == 0) cnt[slot] = 0;
-      // unit completion
-      int old = 0;
+    float* rs = S.red + rs_slot * (SR * S.NS * MAX_GROUP);
+    reduce_to_red<C, WPS, N>(v, pos, SR, S.NS, rs);
+    if (stage_arrive_last(&S.cnt[rs_slot], S.nwc, pos.lane)) {
+      if (!red_slot_wait(&useq[ui % NUB], ui, S.abort_flag)) {
+        if (pos.lane == 0) {
+          *S.abort_flag = 1;
+          flag_status(S.status, DEV_TIMEOUT_PIPE);
+        }
+        dead = true;
+        continue;
+      }
+      stage_final<C>(rs, SR, S.NS, pos.lane,
+                     [&](int row, int c, float val) { ub[(s * SR + row) * MAX_GROUP + c] = val; });
       __syncwarp();
+      int old = 0;
       if (pos.lane == 0) {
+        S.cnt[rs_slot] = 0;
         __threadfence_block();
-        old = atomicAdd(&ucnt[ui % nub], 1);
+        S.seq[rs_slot] = it + NRED;
+        old = atomicAdd(&ucnt[ui % NUB], 1);
       }
       old = __shfl_sync(0xffffffffu, old, 0);
-      if (old == 7) {
+      if (old == 7) {  // the unit's eighth stage: SwiGLU + q8_1
         __threadfence_block();
         gu_epilogue<C>(a, G, g, ib, ub, pos.lane);
-        if (pos.lane == 0) ucnt[ui % nub] = 0;
+        __syncwarp();
+        if (pos.lane == 0) {
+          ucnt[ui % NUB] = 0;
+          __threadfence_block();
+          useq[ui % NUB] = ui + NUB;
+        }
       }
-      __syncwarp();
     }
-    if (pos.lane == 0) mbar_arrive(&empty[slot]);
   }
 }
 
-template <int WPS>
-__global__ void __launch_bounds__(512, 1) moe_gu_kernel(DecodeArgs a) {
+template <int WPS, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1) moe_gu_kernel(DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  using R = Ring<MOEX_Q8_0, WPS>;
   const int NB = a.H / QK;
   const int NS = num_slices(NB);
-  const GuSmem L(a.T, a.H, NS, a.nst, a.stage_bytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* empty = full + a.nst;
+  const int nwc = NS * WPS;
+  const int slot_bytes = R::slot_bytes(nwc);
+  const GuSmem L(a.T, a.H, NS, a.nst, slot_bytes);
   int* cnt = reinterpret_cast<int*>(smem + L.cnt);
+  volatile int* seq = reinterpret_cast<volatile int*>(smem + L.seq);
+  volatile int* useq = reinterpret_cast<volatile int*>(smem + L.useq);
   int* ucnt = reinterpret_cast<int*>(smem + L.ucnt);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
   Groups& G = *reinterpret_cast<Groups*>(smem + L.groups);
   int8_t* xs = reinterpret_cast<int8_t*>(smem + L.xs);
   float* xd = reinterpret_cast<float*>(smem + L.xd);
-  float* red = reinterpret_cast<float*>(smem + L.red);
   float* ubuf = reinterpret_cast<float*>(smem + L.ubuf);
-  uint8_t* stages = smem + L.stages;
+  uint8_t* ring = smem + L.ring;
 
-  const int nwc = NS * WPS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const ConsumerPos pos = consumer_pos(warp, lane, WPS);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < a.nst; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], nwc);
+    for (int i = 0; i < NRED; ++i) {
       cnt[i] = 0;
+      seq[i] = i;
     }
-    for (int i = 0; i < L.nub; ++i) ucnt[i] = 0;
+    for (int i = 0; i < NUB; ++i) {
+      ucnt[i] = 0;
+      useq[i] = i;
+    }
     *abort_flag = 0;
-    fence_mbar_init();
   }
   pdl_wait();  // routing ids and the layer input come from earlier kernels
   if (threadIdx.x == 0) build_groups(G, a.ids, a.n, a.E, a.status);
@@ -274,72 +305,73 @@ __global__ void __launch_bounds__(512, 1) moe_gu_kernel(DecodeArgs a) {
   const int ib_per = a.I / QK;
   const int units = G.ng * ib_per;
   const int nunit = units > static_cast<int>(blockIdx.x) ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-
-  if (warp == nwc) {
-    if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();
-      int issued = 0;
-      for (int ui = 0; ui < nunit && !*abort_flag; ++ui) {
-        const int u = blockIdx.x + ui * gridDim.x;
-        const int g = u / ib_per, ib = u % ib_per;
-        const int64_t mat_row0 = static_cast<int64_t>(G.gexp[g]) * 2 * a.I;
-        for (int s = 0; s < 8; ++s) {
-          const int it = ui * 8 + s;
-          const int slot = it % a.nst;
-          if (it >= a.nst && !mbar_wait(&empty[slot], ((it / a.nst) - 1) & 1, abort_flag)) {
-            *abort_flag = 1;
-            flag_status(a.status, DEV_TIMEOUT_PIPE);
-            break;
-          }
-          const int64_t r0 = mat_row0 + (s < 4 ? ib * QK + s * SR : a.I + ib * QK + (s - 4) * SR);
-          uint8_t* st = stages + static_cast<size_t>(slot) * a.stage_bytes;
-          mbar_arrive_expect_tx(&full[slot], SR * (a.gu_qrow + a.gu_scrow));
-          bulk_g2s_stream(st, a.gu_qs + r0 * a.gu_qrow, SR * a.gu_qrow, &full[slot], pol);
-          bulk_g2s_stream(st + SR * a.gu_qrow, a.gu_sc + r0 * a.gu_scrow, SR * a.gu_scrow, &full[slot], pol);
-          issued = it + 1;
+  const int nstage = nunit * 8;
+  auto unit_rows = [&](int ui, int s) {
+    const int u = blockIdx.x + ui * gridDim.x;
+    const int g = u / ib_per, ib = u % ib_per;
+    const int64_t mat_row0 = static_cast<int64_t>(G.gexp[g]) * 2 * a.I;
+    return mat_row0 + (s < 4 ? ib * QK + s * SR : a.I + ib * QK + (s - 4) * SR);
+  };
+  auto issue = [&](int it) {
+    if (it < nstage) {
+      const int64_t r0 = unit_rows(it / 8, it % 8);
+      ring_issue<MOEX_Q8_0, WPS>(ring + static_cast<size_t>(it % a.nst) * slot_bytes, nwc, pos,
+                                 a.gu_qs + r0 * a.gu_qrow, a.gu_sc + r0 * a.gu_scrow, SR, a.gu_qrow, a.gu_scrow, NB);
+      // one unit ahead of the ring: ask for the following unit in L2
+      if (it % 8 == 0 && threadIdx.x == 0 && it / 8 + 1 < nunit) {
+        for (int half = 0; half < 2; ++half) {
+          const int64_t p0 = unit_rows(it / 8 + 1, half * 4);
+          prefetch_l2(a.gu_qs + p0 * a.gu_qrow, 32 * static_cast<int64_t>(a.gu_qrow));
+          prefetch_l2(a.gu_sc + p0 * a.gu_scrow, 32 * static_cast<int64_t>(a.gu_scrow));
         }
       }
-      if (*abort_flag) {
-        for (int it = max(0, issued - a.nst); it < issued; ++it)
-          mbar_wait(&full[it % a.nst], (it / a.nst) & 1, nullptr);
-      }
     }
-    return;
-  }
+    cp_async_commit();
+  };
+  for (int it = 0; it < a.nst; ++it) issue(it);
 
-  ConsumerPos pos;
-  pos.ks = warp / WPS;
-  pos.jw = warp % WPS;
-  pos.lane = lane;
-  pos.hf = lane >> 4;
-  pos.li = lane & 15;
+  StageCtx S;
+  S.ring = ring;
+  S.slot_bytes = slot_bytes;
+  S.nst = a.nst;
+  S.nwc = nwc;
+  S.NS = NS;
+  S.NB = NB;
+  S.cnt = cnt;
+  S.seq = seq;
+  S.abort_flag = abort_flag;
+  S.red = reinterpret_cast<float*>(smem + L.red);
+  S.status = a.status;
   bool dead = false;
   for (int ui = 0; ui < nunit; ++ui) {
     const int u = blockIdx.x + ui * gridDim.x;
     const int g = u / ib_per, ib = u % ib_per;
     const int m = G.gstart[g + 1] - G.gstart[g];
+#define MOEX_GU(CC) gu_unit<CC, WPS>(a, G, g, ib, ui, ui * 8, S, pos, xs, xd, ucnt, useq, ubuf, dead, issue)
     switch (m) {
-      case 1: gu_unit<1, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
-      case 2: gu_unit<2, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
-      case 3: gu_unit<3, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
-      case 4: gu_unit<4, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
-      case 5: gu_unit<5, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
-      case 6: gu_unit<6, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
-      case 7: gu_unit<7, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
-      default: gu_unit<8, WPS>(a, G, g, ib, ui, NB, NS, nwc, pos, xs, xd, full, empty, cnt, ucnt, red, ubuf, L.nub, stages, abort_flag, dead); break;
+      case 1: MOEX_GU(1); break;
+      case 2: MOEX_GU(2); break;
+      case 3: MOEX_GU(3); break;
+      case 4: MOEX_GU(4); break;
+      case 5: MOEX_GU(5); break;
+      case 6: MOEX_GU(6); break;
+      case 7: MOEX_GU(7); break;
+      default: MOEX_GU(8); break;
     }
+#undef MOEX_GU
   }
+  cp_async_wait(0);
 }
 
 // ============================================================== down + combine
 
 struct DnSmem {
-  int bars, cnt, abort_flag, groups, hs, hd, red, osum, stages, total;
-  __host__ __device__ DnSmem(int n, int I, int NS, int rows_max, int nst, int stage_bytes) {
+  int cnt, seq, abort_flag, groups, hs, hd, red, osum, ring, total;
+  __host__ __device__ DnSmem(int n, int I, int NS, int rows_max, int nst, int slot_bytes) {
     const int NB = I / QK;
     int o = 0;
-    bars = o; o += 16 * nst;
-    cnt = o; o += 4 * nst;
+    cnt = o; o += 4 * NRED;
+    seq = o; o += 4 * NRED;
     abort_flag = o; o += 16;
     o = (o + 15) & ~15;
     groups = o; o += static_cast<int>(sizeof(Groups));
@@ -348,10 +380,10 @@ struct DnSmem {
     o = (o + 15) & ~15;
     hd = o; o += 4 * n * NB;
     o = (o + 15) & ~15;
-    red = o; o += 4 * nst * SR * NS * MAX_GROUP;
+    red = o; o += 4 * NRED * SR * NS * MAX_GROUP;
     osum = o; o += 4 * n * rows_max;
     o = (o + 127) & ~127;
-    stages = o; o += nst * stage_bytes;
+    ring = o; o += nst * slot_bytes;
     total = o;
   }
 };
@@ -360,11 +392,10 @@ struct DnSmem {
 // of balanced size; stage s covers rows [s*nrows/ns, (s+1)*nrows/ns).
 __device__ __forceinline__ int dn_nstages(int nrows) { return (nrows + SR - 1) / SR; }
 
-template <int FMT, int C, int WPS>
-__device__ __forceinline__ void dn_group(const DecodeArgs& a, const Groups& G, int g, int it0, int nrows, int NB,
-                                         int NS, int nwc, const ConsumerPos& pos, const int8_t* hs, const float* hd,
-                                         uint64_t* full, uint64_t* empty, int* cnt, float* red, float* osum,
-                                         int rows_max, const uint8_t* stages, volatile int* abort_flag, bool& dead) {
+template <int FMT, int C, int WPS, typename Issue>
+__device__ __forceinline__ void dn_group(const DecodeArgs& a, const Groups& G, int g, int it0, int nrows,
+                                         const StageCtx& S, const ConsumerPos& pos, const int8_t* hs, const float* hd,
+                                         float* osum, int rows_max, bool& dead, Issue&& issue) {
   ActRegs<FMT, C> act;
   {
     const int8_t* xcol[C];
@@ -373,112 +404,109 @@ __device__ __forceinline__ void dn_group(const DecodeArgs& a, const Groups& G, i
     for (int c = 0; c < C; ++c) {
       const int j = G.ent[G.gstart[g] + c];
       xcol[c] = hs + j * a.I;
-      dcol[c] = hd + j * NB;
+      dcol[c] = hd + j * S.NB;
     }
     const int b = pos.ks * SLICE + pos.li;
-    load_act<FMT, C>(act, xcol, dcol, b, b < NB, pos.li);
+    load_act<FMT, C>(act, xcol, dcol, b, b < S.NB, pos.li);
   }
+  constexpr int N = Vals<C, WPS>::N;
   const int ns = dn_nstages(nrows);
   for (int s = 0; s < ns; ++s) {
     const int it = it0 + s;
-    const int slot = it % a.nst;
-    if (!dead && !mbar_wait(&full[slot], (it / a.nst) & 1, abort_flag)) {
+    const int rlo = s * nrows / ns, rhi = (s + 1) * nrows / ns;
+    cp_async_wait(S.nst - 1);
+    float v[N];
+    if (!dead) ring_partials<FMT, C, WPS, N>(S.ring + static_cast<size_t>(it % S.nst) * S.slot_bytes, S.nwc, pos,
+                                             rhi - rlo, S.NB, act, v);
+    issue(it + S.nst);
+    if (dead) continue;
+    const int rs_slot = it % NRED;
+    if (!red_slot_wait(&S.seq[rs_slot], it, S.abort_flag)) {
       if (pos.lane == 0) {
-        *abort_flag = 1;
-        flag_status(a.status, DEV_TIMEOUT_PIPE);
+        *S.abort_flag = 1;
+        flag_status(S.status, DEV_TIMEOUT_PIPE);
       }
       dead = true;
+      continue;
     }
-    if (dead) continue;
-    const int rlo = s * nrows / ns, rhi = (s + 1) * nrows / ns;
-    const uint8_t* stage = stages + static_cast<size_t>(slot) * a.stage_bytes;
-    float* rs = red + slot * (SR * NS * MAX_GROUP);
-    stage_partials<FMT, C, WPS>(stage, stage + SR * a.dn_qrow, a.dn_qrow, a.dn_scrow, rhi - rlo, NB, NS, pos, act,
-                                rs);
-    if (stage_arrive_last(&cnt[slot], nwc, pos.lane)) {
+    float* rs = S.red + rs_slot * (SR * S.NS * MAX_GROUP);
+    reduce_to_red<C, WPS, N>(v, pos, rhi - rlo, S.NS, rs);
+    if (stage_arrive_last(&S.cnt[rs_slot], S.nwc, pos.lane)) {
       const int gbase = G.gstart[g];
-      stage_final<C>(rs, rhi - rlo, NS, pos.lane, [&](int row, int c, float v) {
-        osum[G.ent[gbase + c] * rows_max + rlo + row] = v;
+      stage_final<C>(rs, rhi - rlo, S.NS, pos.lane, [&](int row, int c, float val) {
+        osum[G.ent[gbase + c] * rows_max + rlo + row] = val;
       });
-      if (pos.lane == 0) cnt[slot] = 0;
       __syncwarp();
+      if (pos.lane == 0) {
+        S.cnt[rs_slot] = 0;
+        __threadfence_block();
+        S.seq[rs_slot] = it + NRED;
+      }
     }
-    if (pos.lane == 0) mbar_arrive(&empty[slot]);
   }
 }
 
-template <int FMT, int WPS>
-__global__ void __launch_bounds__(512, 1) moe_dn_kernel(DecodeArgs a) {
+template <int FMT, int WPS, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  using R = Ring<FMT, WPS>;
   const int NB = a.I / QK;
   const int NS = num_slices(NB);
+  const int nwc = NS * WPS;
+  const int slot_bytes = R::slot_bytes(nwc);
   const int G_ = gridDim.x;
   const int rows_max = (a.H + G_ - 1) / G_;
-  const DnSmem L(a.n, a.I, NS, rows_max, a.nst, a.stage_bytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* empty = full + a.nst;
+  const DnSmem L(a.n, a.I, NS, rows_max, a.nst, slot_bytes);
   int* cnt = reinterpret_cast<int*>(smem + L.cnt);
+  volatile int* seq = reinterpret_cast<volatile int*>(smem + L.seq);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
   Groups& G = *reinterpret_cast<Groups*>(smem + L.groups);
   int8_t* hs = reinterpret_cast<int8_t*>(smem + L.hs);
   float* hd = reinterpret_cast<float*>(smem + L.hd);
-  float* red = reinterpret_cast<float*>(smem + L.red);
   float* osum = reinterpret_cast<float*>(smem + L.osum);
-  const uint8_t* stages = smem + L.stages;
+  uint8_t* ring = smem + L.ring;
 
-  const int nwc = NS * WPS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const ConsumerPos pos = consumer_pos(warp, lane, WPS);
   const int row_begin = static_cast<int>(static_cast<int64_t>(a.H) * blockIdx.x / G_);
   const int row_end = static_cast<int>(static_cast<int64_t>(a.H) * (blockIdx.x + 1) / G_);
   const int nrows = row_end - row_begin;
+  const int ns = dn_nstages(nrows);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < a.nst; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], nwc);
+    for (int i = 0; i < NRED; ++i) {
       cnt[i] = 0;
+      seq[i] = i;
     }
     *abort_flag = 0;
-    fence_mbar_init();
     // The routing ids were complete before the gate/up kernel let this grid
     // launch, so they are read before griddepcontrol.wait.
     build_groups(G, a.ids, a.n, a.E, nullptr);
   }
   __syncthreads();
+  const int nstage = G.ng * ns;
+  if (threadIdx.x == 0) {
+    // the CTA's whole share of the routed experts' rows into L2
+    for (int g = 0; g < G.ng; ++g) {
+      const int64_t r0 = static_cast<int64_t>(G.gexp[g]) * a.H + row_begin;
+      prefetch_l2(a.dn_qs + r0 * a.dn_qrow, static_cast<int64_t>(nrows) * a.dn_qrow);
+      prefetch_l2(a.dn_sc + r0 * a.dn_scrow, static_cast<int64_t>(nrows) * a.dn_scrow);
+    }
+  }
+  auto issue = [&](int it) {
+    if (it < nstage) {
+      const int g = it / ns, s = it % ns;
+      const int rlo = s * nrows / ns, rhi = (s + 1) * nrows / ns;
+      const int64_t r0 = static_cast<int64_t>(G.gexp[g]) * a.H + row_begin + rlo;
+      ring_issue<FMT, WPS>(ring + static_cast<size_t>(it % a.nst) * slot_bytes, nwc, pos, a.dn_qs + r0 * a.dn_qrow,
+                           a.dn_sc + r0 * a.dn_scrow, rhi - rlo, a.dn_qrow, a.dn_scrow, NB);
+    }
+    cp_async_commit();
+  };
+  for (int it = 0; it < a.nst; ++it) issue(it);
   pdl_launch_dependents();
 
-  if (warp == nwc) {
-    if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();
-      const int ns = dn_nstages(nrows);
-      int it = 0, issued = 0;
-      for (int g = 0; g < G.ng && !*abort_flag; ++g) {
-        const int64_t mat_row0 = static_cast<int64_t>(G.gexp[g]) * a.H + row_begin;
-        for (int s = 0; s < ns; ++s, ++it) {
-          const int slot = it % a.nst;
-          if (it >= a.nst && !mbar_wait(&empty[slot], ((it / a.nst) - 1) & 1, abort_flag)) {
-            *abort_flag = 1;
-            flag_status(a.status, DEV_TIMEOUT_PIPE);
-            break;
-          }
-          const int rlo = s * nrows / ns, rhi = (s + 1) * nrows / ns;
-          const int64_t r0 = mat_row0 + rlo;
-          const int n = rhi - rlo;
-          uint8_t* st = const_cast<uint8_t*>(stages) + static_cast<size_t>(slot) * a.stage_bytes;
-          mbar_arrive_expect_tx(&full[slot], n * (a.dn_qrow + a.dn_scrow));
-          bulk_g2s_stream(st, a.dn_qs + r0 * a.dn_qrow, n * a.dn_qrow, &full[slot], pol);
-          bulk_g2s_stream(st + SR * a.dn_qrow, a.dn_sc + r0 * a.dn_scrow, n * a.dn_scrow, &full[slot], pol);
-          issued = it + 1;
-        }
-      }
-      if (*abort_flag) {
-        for (int i = max(0, issued - a.nst); i < issued; ++i) mbar_wait(&full[i % a.nst], (i / a.nst) & 1, nullptr);
-      }
-    }
-    return;
-  }
-
-  // consumers: Hq of every entry into shared memory, after the gate/up grid
+  // Hq of every entry into shared memory, after the gate/up grid
   pdl_wait();
   const int nthr = nwc * 32;
   {
@@ -488,21 +516,24 @@ __global__ void __launch_bounds__(512, 1) moe_dn_kernel(DecodeArgs a) {
     const float2* dsrc = reinterpret_cast<const float2*>(a.hds);
     for (int i = threadIdx.x; i < a.n * NB; i += nthr) hd[i] = dsrc[i].x;
     for (int i = threadIdx.x; i < a.n * rows_max; i += nthr) osum[i] = 0.f;
-    named_bar_sync(1, nthr);
+    __syncthreads();
   }
-  ConsumerPos pos;
-  pos.ks = warp / WPS;
-  pos.jw = warp % WPS;
-  pos.lane = lane;
-  pos.hf = lane >> 4;
-  pos.li = lane & 15;
+  StageCtx S;
+  S.ring = ring;
+  S.slot_bytes = slot_bytes;
+  S.nst = a.nst;
+  S.nwc = nwc;
+  S.NS = NS;
+  S.NB = NB;
+  S.cnt = cnt;
+  S.seq = seq;
+  S.abort_flag = abort_flag;
+  S.red = reinterpret_cast<float*>(smem + L.red);
+  S.status = a.status;
   bool dead = false;
-  const int ns = dn_nstages(nrows);
   for (int g = 0; g < G.ng; ++g) {
     const int m = G.gstart[g + 1] - G.gstart[g];
-    const int it0 = g * ns;
-#define MOEX_DN(CC) \
-  dn_group<FMT, CC, WPS>(a, G, g, it0, nrows, NB, NS, nwc, pos, hs, hd, full, empty, cnt, red, osum, rows_max, stages, abort_flag, dead)
+#define MOEX_DN(CC) dn_group<FMT, CC, WPS>(a, G, g, g * ns, nrows, S, pos, hs, hd, osum, rows_max, dead, issue)
     switch (m) {
       case 1: MOEX_DN(1); break;
       case 2: MOEX_DN(2); break;
@@ -515,7 +546,8 @@ __global__ void __launch_bounds__(512, 1) moe_dn_kernel(DecodeArgs a) {
     }
 #undef MOEX_DN
   }
-  named_bar_sync(1, nthr);
+  cp_async_wait(0);
+  __syncthreads();
   // combine: out[t][r] = sum over slots in order of w[t,slot] * o[(t,slot)][r]
   for (int i = threadIdx.x; i < a.T * nrows; i += nthr) {
     const int t = i / nrows, rl = i % nrows;
@@ -541,52 +573,54 @@ size_t moe_decode_ws_bytes(int T, int k, int64_t hidden, int64_t inter) {
 
 namespace {
 
-template <int WPS>
+template <int WPS, int MAXT>
 moex_status launch_gu(const DecodeArgs& base, int smem_cap, cudaStream_t s) {
   DecodeArgs a = base;
   const int NB = a.H / QK, NS = num_slices(NB);
-  a.stage_bytes = ((SR * (a.gu_qrow + a.gu_scrow)) + 127) & ~127;
-  int nst = 16;
+  const int slot_bytes = Ring<MOEX_Q8_0, WPS>::slot_bytes(NS * WPS);
+  int nst = 8;
   for (; nst >= 2; --nst)
-    if (GuSmem(a.T, a.H, NS, nst, a.stage_bytes).total <= smem_cap) break;
+    if (GuSmem(a.T, a.H, NS, nst, slot_bytes).total <= smem_cap) break;
   if (nst < 2) return MOEX_EUNSUPPORTED;
   a.nst = nst;
-  const GuSmem L(a.T, a.H, NS, nst, a.stage_bytes);
-  auto kern = moe_gu_kernel<WPS>;
+  const GuSmem L(a.T, a.H, NS, nst, slot_bytes);
+  auto kern = moe_gu_kernel<WPS, MAXT>;
   if (ensure_smem(reinterpret_cast<const void*>(kern), L.total) != cudaSuccess) return MOEX_ECUDA;
   // grid: enough CTAs for the largest possible unit count is not known on
   // the host (it depends on the routing); use every SM.
   const int grid = sm_count();
-  const int threads = (NS * WPS + 1) * 32;
+  const int threads = NS * WPS * 32;
   return cuda_status(launch_pdl(kern, dim3(grid), dim3(threads), L.total, s, a));
 }
 
-template <int FMT, int WPS>
+template <int FMT, int WPS, int MAXT>
 moex_status launch_dn(const DecodeArgs& base, int smem_cap, cudaStream_t s) {
   DecodeArgs a = base;
   const int NB = a.I / QK, NS = num_slices(NB);
-  a.stage_bytes = ((SR * (a.dn_qrow + a.dn_scrow)) + 127) & ~127;
+  const int slot_bytes = Ring<FMT, WPS>::slot_bytes(NS * WPS);
   const int grid = a.H < sm_count() ? a.H : sm_count();
   const int rows_max = (a.H + grid - 1) / grid;
-  int nst = 16;
+  int nst = 8;
   for (; nst >= 2; --nst)
-    if (DnSmem(a.n, a.I, NS, rows_max, nst, a.stage_bytes).total <= smem_cap) break;
+    if (DnSmem(a.n, a.I, NS, rows_max, nst, slot_bytes).total <= smem_cap) break;
   if (nst < 2) return MOEX_EUNSUPPORTED;
   a.nst = nst;
-  const DnSmem L(a.n, a.I, NS, rows_max, nst, a.stage_bytes);
-  auto kern = moe_dn_kernel<FMT, WPS>;
+  const DnSmem L(a.n, a.I, NS, rows_max, nst, slot_bytes);
+  auto kern = moe_dn_kernel<FMT, WPS, MAXT>;
   if (ensure_smem(reinterpret_cast<const void*>(kern), L.total) != cudaSuccess) return MOEX_ECUDA;
-  const int threads = (NS * WPS + 1) * 32;
+  const int threads = NS * WPS * 32;
   return cuda_status(launch_pdl(kern, dim3(grid), dim3(threads), L.total, s, a));
 }
 
+// Decode kernels: two warps per K slice up to 8 slices (K <= 4096), else one.
+inline int decode_wps(int NS) { return NS <= 8 ? 2 : 1; }
+
 template <int FMT>
 moex_status launch_dn_fmt(const DecodeArgs& a, int cap, cudaStream_t s) {
-  switch (warps_per_slice(num_slices(a.I / QK))) {
-    case 4: return launch_dn<FMT, 4>(a, cap, s);
-    case 2: return launch_dn<FMT, 2>(a, cap, s);
-    default: return launch_dn<FMT, 1>(a, cap, s);
-  }
+  const int NS = num_slices(a.I / QK);
+  const int wps = decode_wps(NS);
+  if (wps == 2) return NS * 2 * 32 <= 320 ? launch_dn<FMT, 2, 320>(a, cap, s) : launch_dn<FMT, 2, 512>(a, cap, s);
+  return NS * 32 <= 320 ? launch_dn<FMT, 1, 320>(a, cap, s) : launch_dn<FMT, 1, 512>(a, cap, s);
 }
 
 }  // namespace
@@ -623,13 +657,12 @@ moex_status launch_moe_decode(const moex_qweight* gu, const moex_qweight* dn, co
   a.status = device_status_ptr();
   const int cap = max_smem_optin();
   const int NSg = num_slices(a.H / QK), NSd = num_slices(a.I / QK);
-  if (NSg * warps_per_slice(NSg) > 15 || NSd * warps_per_slice(NSd) > 15) return MOEX_EUNSUPPORTED;
+  if (NSg > 16 || NSd > 16) return MOEX_EUNSUPPORTED;
   moex_status st;
-  switch (warps_per_slice(NSg)) {
-    case 4: st = launch_gu<4>(a, cap, s); break;
-    case 2: st = launch_gu<2>(a, cap, s); break;
-    default: st = launch_gu<1>(a, cap, s); break;
-  }
+  if (decode_wps(NSg) == 2)
+    st = NSg * 64 <= 320 ? launch_gu<2, 320>(a, cap, s) : launch_gu<2, 512>(a, cap, s);
+  else
+    st = NSg * 32 <= 320 ? launch_gu<1, 320>(a, cap, s) : launch_gu<1, 512>(a, cap, s);
   if (st != MOEX_OK) return st;
   return dn->fmt == MOEX_Q8_0 ? launch_dn_fmt<MOEX_Q8_0>(a, cap, s) : launch_dn_fmt<MOEX_IQ4_NL>(a, cap, s);
 }

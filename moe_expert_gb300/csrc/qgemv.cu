@@ -17,7 +17,7 @@ struct GemvArgs {
   int K, NB, NS;        // inputs, blocks, K slices
   int qrow, scrow;      // plane row strides (bytes)
   int nst;              // ring slots
-  int stage_bytes;      // bytes of one ring slot
+  int stage_bytes;      // unused
   const int8_t* xq;     // q8_1 quants [ncols][K]
   const float* xds;     // {d, s} [ncols][NB]
   float* y;
@@ -25,142 +25,227 @@ struct GemvArgs {
   uint32_t* status;
 };
 
-// Shared-memory carve-up of the dense GEMV (all offsets 16-byte aligned;
-// stage slots 128-byte aligned).
+
+
+// Shared-memory carve-up of the dense GEMV.
 struct GemvSmem {
-  int bars, cnt, abort_flag, xs, xd, red, stages, total;
-  __host__ __device__ GemvSmem(int C, int K, int NB, int NS, int nst, int stage_bytes) {
+  int cnt, seq, abort_flag, red, ring, total;
+  __host__ __device__ GemvSmem(int C, int NS, int nst, int slot_bytes) {
     int o = 0;
-    bars = o; o += 16 * nst;
-    cnt = o; o += 4 * nst;
+    cnt = o; o += 4 * NRED;
+    seq = o; o += 4 * NRED;
     abort_flag = o; o += 16;
     o = (o + 15) & ~15;
-    xs = o; o += C * K;
-    o = (o + 15) & ~15;
-    xd = o; o += 4 * C * NB;
-    o = (o + 15) & ~15;
-    red = o; o += 4 * nst * SR * NS * C;
+    red = o; o += 4 * NRED * SR * NS * C;
     o = (o + 127) & ~127;
-    stages = o; o += nst * stage_bytes;
+    ring = o; o += nst * slot_bytes;
     total = o;
   }
 };
 
-template <int FMT, int C, int WPS>
-__global__ void __launch_bounds__(512, 1) qgemv_kernel(GemvArgs a) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const GemvSmem L(C, a.K, a.NB, a.NS, a.nst, a.stage_bytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* empty = full + a.nst;
-  int* cnt = reinterpret_cast<int*>(smem + L.cnt);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
-  int8_t* xs = reinterpret_cast<int8_t*>(smem + L.xs);
-  float* xd = reinterpret_cast<float*>(smem + L.xd);
-  float* red = reinterpret_cast<float*>(smem + L.red);
-  uint8_t* stages = smem + L.stages;
+// Threads of a dense GEMV CTA: NS*WPS warps.  MINB == 2 variants keep
+// registers and shared memory small enough that a CTA of the next GEMV in the
+// stream is resident beside this one, so with programmatic dependent launch
+// its weight stream starts while this one drains.
+template <int WPS, int MINB>
+struct GemvBounds {
+  static constexpr int MAXT = MINB == 2 ? 5 * WPS * 32 : 512;
+};
 
-  const int nwc = a.NS * WPS;  // consumer warps
+// Every CTA owns a contiguous range of rows.  At entry one thread asks for
+// the whole range in L2 (cp.async.bulk.prefetch.L2) and every lane issues
+// its cp.async copies for the first `nst` stages; all of that happens before
+// griddepcontrol.wait, since the weights do not depend on the previous
+// kernel.  Then the activation blocks are loaded straight into registers and
+// the stages are consumed in order, each slot refilled as soon as its lane
+// has read it.  The partial sums of a stage are reduced over the half warp,
+// then over the K slices by the last warp to finish the stage.
+template <int FMT, int C, int WPS, int MINB>
+__global__ void __launch_bounds__(GemvBounds<WPS, MINB>::MAXT, MINB) qgemv_kernel(GemvArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  MOEX_TRACE_BEGIN();
+  using R = Ring<FMT, WPS>;
+  const int nwc = a.NS * WPS;
+  const int slot_bytes = R::slot_bytes(nwc);
+  const GemvSmem L(C, a.NS, a.nst, slot_bytes);
+  int* cnt = reinterpret_cast<int*>(smem + L.cnt);
+  volatile int* seq = reinterpret_cast<volatile int*>(smem + L.seq);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  uint8_t* ring = smem + L.ring;
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const ConsumerPos pos = consumer_pos(warp, lane, WPS);
   const int64_t G = gridDim.x;
   const int64_t row_begin = a.rows * blockIdx.x / G;
   const int64_t row_end = a.rows * (blockIdx.x + 1) / G;
   const int nstage = static_cast<int>((row_end - row_begin + SR - 1) / SR);
+  auto stage_rows = [&](int it) {
+    const int64_t r0 = row_begin + static_cast<int64_t>(it) * SR;
+    return static_cast<int>((row_end - r0) < SR ? (row_end - r0) : SR);
+  };
+  auto issue = [&](int it) {
+    if (it < nstage) {
+      const int64_t r0 = row_begin + static_cast<int64_t>(it) * SR;
+      ring_issue<FMT, WPS>(ring + static_cast<size_t>(it % a.nst) * slot_bytes, nwc, pos, a.qs + r0 * a.qrow,
+                           a.sc + r0 * a.scrow, stage_rows(it), a.qrow, a.scrow, a.NB);
+    }
+    cp_async_commit();
+  };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < a.nst; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], nwc);
+    for (int i = 0; i < NRED; ++i) {
       cnt[i] = 0;
+      seq[i] = i;
     }
     *abort_flag = 0;
-    fence_mbar_init();
   }
   __syncthreads();
+  MOEX_TRACE_STAMP(0);
+  for (int it = 0; it < a.nst; ++it) issue(it);
+  // the stages beyond the ring: into L2 now, before waiting for the previous kernel
+  for (int it = a.nst; it < nstage; ++it) {
+    const int64_t r0 = row_begin + static_cast<int64_t>(it) * SR;
+    lane_prefetch_l2<FMT, WPS>(pos, a.qs + r0 * a.qrow, a.sc + r0 * a.scrow, stage_rows(it), a.qrow, a.scrow, a.NB);
+  }
+  MOEX_TRACE_STAMP(1);
   pdl_launch_dependents();
-
-  if (warp == nwc) {
-    // ---------------- producer: stream the CTA's rows (weights only; they do
-    // not depend on the previous kernel, so no griddepcontrol.wait here).
-    if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();
-      int issued = 0;
-      for (int it = 0; it < nstage; ++it) {
-        const int slot = it % a.nst;
-        if (it >= a.nst && !mbar_wait(&empty[slot], ((it / a.nst) - 1) & 1, abort_flag)) {
-          *abort_flag = 1;
-          flag_status(a.status, DEV_TIMEOUT_PIPE);
-          break;
-        }
-        const int64_t r0 = row_begin + static_cast<int64_t>(it) * SR;
-        const int n = static_cast<int>((row_end - r0) < SR ? (row_end - r0) : SR);
-        uint8_t* st = stages + static_cast<size_t>(slot) * a.stage_bytes;
-        mbar_arrive_expect_tx(&full[slot], n * (a.qrow + a.scrow));
-        bulk_g2s_stream(st, a.qs + r0 * a.qrow, n * a.qrow, &full[slot], pol);
-        bulk_g2s_stream(st + SR * a.qrow, a.sc + r0 * a.scrow, n * a.scrow, &full[slot], pol);
-        issued = it + 1;
-      }
-      // On abort, wait (bounded) for copies still landing in this CTA's smem.
-      if (*abort_flag) {
-        for (int it = max(0, issued - a.nst); it < issued; ++it)
-          mbar_wait(&full[it % a.nst], (it / a.nst) & 1, nullptr);
-      }
-    }
-    return;
-  }
-
-  // ---------------- consumers
   pdl_wait();  // activations come from the previous kernel
-  {
-    const int nthr = nwc * 32;
-    const int4* src = reinterpret_cast<const int4*>(a.xq);
-    int4* dst = reinterpret_cast<int4*>(xs);
-    for (int i = threadIdx.x; i < C * a.K / 16; i += nthr) dst[i] = src[i];
-    const float2* dsrc = reinterpret_cast<const float2*>(a.xds);
-    for (int i = threadIdx.x; i < C * a.NB; i += nthr) xd[i] = dsrc[i].x;
-    named_bar_sync(1, nthr);
-  }
-  ConsumerPos pos;
-  pos.ks = warp / WPS;
-  pos.jw = warp % WPS;
-  pos.lane = lane;
-  pos.hf = lane >> 4;
-  pos.li = lane & 15;
-  const int b = pos.ks * SLICE + pos.li;
+  MOEX_TRACE_STAMP(2);
   ActRegs<FMT, C> act;
   {
     const int8_t* xcol[C];
     const float* dcol[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) {
-      xcol[c] = xs + c * a.K;
-      dcol[c] = xd + c * a.NB;
+      xcol[c] = a.xq + static_cast<int64_t>(c) * a.K;
+      dcol[c] = a.xds + static_cast<int64_t>(c) * a.NB * 2;
     }
-    load_act<FMT, C>(act, xcol, dcol, b, b < a.NB, pos.li);
+    const int b = pos.ks * SLICE + pos.li;
+    load_act<FMT, C>(act, xcol, dcol, b, b < a.NB, pos.li, 2);
   }
+  MOEX_TRACE_STAMP(3);
 
+  constexpr int N = Vals<C, WPS>::N;
   for (int it = 0; it < nstage; ++it) {
-    const int slot = it % a.nst;
-    const bool ok = mbar_wait(&full[slot], (it / a.nst) & 1, abort_flag);
-    if (!ok) {
+    const int n = stage_rows(it);
+    cp_async_wait(a.nst - 1);
+    if (it == 0) MOEX_TRACE_STAMP(4);
+    float v[N];
+    ring_partials<FMT, C, WPS, N>(ring + static_cast<size_t>(it % a.nst) * slot_bytes, nwc, pos, n, a.NB, act, v);
+    issue(it + a.nst);
+    const int rs_slot = it % NRED;
+    if (!red_slot_wait(&seq[rs_slot], it, abort_flag)) {
       if (lane == 0) {
         *abort_flag = 1;
         flag_status(a.status, DEV_TIMEOUT_PIPE);
       }
       break;
     }
-    const int64_t r0 = row_begin + static_cast<int64_t>(it) * SR;
-    const int n = static_cast<int>((row_end - r0) < SR ? (row_end - r0) : SR);
-    const uint8_t* st = stages + static_cast<size_t>(slot) * a.stage_bytes;
-    float* rs = red + slot * (SR * a.NS * C);
-    stage_partials<FMT, C, WPS>(st, st + SR * a.qrow, a.qrow, a.scrow, n, a.NB, a.NS, pos, act, rs);
-    if (stage_arrive_last(&cnt[slot], nwc, lane)) {
+    float* rs = red + rs_slot * (SR * a.NS * C);
+    reduce_to_red<C, WPS, N>(v, pos, n, a.NS, rs);
+    if (stage_arrive_last(&cnt[rs_slot], nwc, lane)) {
+      const int64_t r0 = row_begin + static_cast<int64_t>(it) * SR;
       float* y = a.y;
       const int64_t ldy = a.ldy;
-      stage_final<C>(rs, n, a.NS, lane, [&](int row, int c, float v) { y[c * ldy + r0 + row] = v; });
-      if (lane == 0) cnt[slot] = 0;
+      stage_final<C>(rs, n, a.NS, lane, [&](int row, int c, float val) { y[c * ldy + r0 + row] = val; });
       __syncwarp();
+      if (lane == 0) {
+        cnt[rs_slot] = 0;
+        __threadfence_block();
+        seq[rs_slot] = it + NRED;
+      }
     }
-    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+  MOEX_TRACE_STAMP(5);
+  cp_async_wait(0);
+}
+
+// ----------------------------------------------------------------- register-staged GEMV
+
+// Small-column variant: every lane loads all of its CTA's weight bytes into
+// registers at entry (plain 16-byte ld.global.nc), before
+// griddepcontrol.wait, so a CTA's whole share of HBM reads is in flight while
+// the previous kernel finishes; nothing of it waits for ring slots or the
+// TMA unit.  Four warps per K slice, one row per half warp per 8-row stage.
+// Partial sums are reduced over the half warp and then over the slices, in
+// slice order, exactly as in the ring variant (same tree: same bits).
+constexpr int REG_WPS = 4;
+
+template <int FMT, int C, int NSTG>
+__global__ void __launch_bounds__(640, 1) qgemv_reg_kernel(GemvArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  using R = Ring<FMT, REG_WPS>;  // geometry only: R::QB, R::NCH
+  float* red = reinterpret_cast<float*>(smem);  // [NSTG*8 rows][NS][C]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const ConsumerPos pos = consumer_pos(warp, lane, REG_WPS);
+  const int64_t G = gridDim.x;
+  const int64_t row_begin = a.rows * blockIdx.x / G;
+  const int64_t row_end = a.rows * (blockIdx.x + 1) / G;
+  const int nrows = static_cast<int>(row_end - row_begin);
+  const int b = pos.ks * SLICE + pos.li;
+  const bool bvalid = b < a.NB;
+  const int my_row0 = pos.jw * 2 + pos.hf;  // row within each stage
+
+  uint4 q[NSTG][R::NCH];
+  uint32_t sw[NSTG];
+#pragma unroll
+  for (int st = 0; st < NSTG; ++st) {
+    const int row = st * SR + my_row0;
+    if (bvalid && row < nrows) {
+      const uint8_t* src = a.qs + (row_begin + row) * a.qrow + b * R::QB;
+#pragma unroll
+      for (int h = 0; h < R::NCH; ++h)
+        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(q[st][h].x), "=r"(q[st][h].y), "=r"(q[st][h].z), "=r"(q[st][h].w)
+                     : "l"(src + 16 * h));
+      asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];"
+                   : "=r"(sw[st])
+                   : "l"(a.sc + (row_begin + row) * a.scrow + 4 * (b >> 1)));
+    } else {
+#pragma unroll
+      for (int h = 0; h < R::NCH; ++h) q[st][h] = make_uint4(0, 0, 0, 0);
+      sw[st] = 0;
+    }
+  }
+  pdl_launch_dependents();
+  pdl_wait();  // activations come from the previous kernel
+  ActRegs<FMT, C> act;
+  {
+    const int8_t* xcol[C];
+    const float* dcol[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      xcol[c] = a.xq + static_cast<int64_t>(c) * a.K;
+      dcol[c] = a.xds + static_cast<int64_t>(c) * a.NB * 2;
+    }
+    load_act<FMT, C>(act, xcol, dcol, b, bvalid, pos.li, 2);
+  }
+  constexpr int N = pow2_ceil(C);
+#pragma unroll
+  for (int st = 0; st < NSTG; ++st) {
+    const int row = st * SR + my_row0;
+    float v[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = 0.f;
+    if (bvalid && row < nrows) {
+      const uint16_t hb = static_cast<uint16_t>((b & 1) ? (sw[st] >> 16) : (sw[st] & 0xFFFFu));
+      block_dots_from<FMT, C>(q[st][0], q[st][R::NCH - 1], __half2float(__ushort_as_half(hb)), act, v);
+    }
+    halving_reduce<N, 8>(v, lane);
+    // lane li holds value li / (16/N) (N < 16 always here)
+    constexpr int REP = 16 / N;
+    if (pos.li % REP == 0) {
+      const int c = pos.li / REP;
+      if (c < C && row < nrows) red[(row * a.NS + pos.ks) * C + c] = v[0];
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < nrows * C; idx += blockDim.x) {
+    const int row = idx / C, c = idx % C;
+    float s = red[(row * a.NS + 0) * C + c];
+    for (int ks = 1; ks < a.NS; ++ks) s = s + red[(row * a.NS + ks) * C + c];
+    a.y[c * a.ldy + row_begin + row] = s;
   }
 }
 
@@ -180,7 +265,7 @@ __global__ void block_dots_kernel(const uint8_t* __restrict__ qs, int64_t rows, 
   load_act<FMT, 1>(act, xcol, nullptr, b, true, li);
   float p;
   int I;
-  block_row_dots<FMT, 1>(qs + r * qrow + static_cast<int64_t>(b) * FmtTraits<FMT>::QBYTES, 1.f, act, li, &p, &I);
+  block_row_dots<FMT, 1>(qs + r * qrow + static_cast<int64_t>(b) * FmtTraits<FMT>::QBYTES, 1.f, act, &p, &I);
   dots[t] = I;
 }
 
@@ -188,31 +273,56 @@ __global__ void block_dots_kernel(const uint8_t* __restrict__ qs, int64_t rows, 
 
 namespace {
 
-template <int FMT, int C, int WPS>
+template <int FMT, int C, int WPS, int MINB>
 moex_status launch_one(const GemvArgs& base, int smem_cap, cudaStream_t s) {
   GemvArgs a = base;
-  auto kern = qgemv_kernel<FMT, C, WPS>;
-  // ring slots: as many as fit, at most 16
-  const GemvSmem l0(C, a.K, a.NB, a.NS, 0, a.stage_bytes);
-  int nst = (smem_cap - l0.total - 256) / (a.stage_bytes + 4 * SR * a.NS * C + 20);
-  nst = nst > 16 ? 16 : nst;
+  auto kern = qgemv_kernel<FMT, C, WPS, MINB>;
+  // ring slots: as many as fit the budget (two CTAs per SM for MINB == 2), at most 8
+  const int budget = MINB == 2 ? 110 * 1024 : smem_cap;
+  const int slot_bytes = Ring<FMT, WPS>::slot_bytes(a.NS * WPS);
+  int nst = 8;
+  for (; nst >= 2; --nst)
+    if (GemvSmem(C, a.NS, nst, slot_bytes).total <= budget) break;
   if (nst < 2) return MOEX_EUNSUPPORTED;
   a.nst = nst;
-  const GemvSmem L(C, a.K, a.NB, a.NS, nst, a.stage_bytes);
+  const GemvSmem L(C, a.NS, nst, slot_bytes);
   if (ensure_smem(reinterpret_cast<const void*>(kern), L.total) != cudaSuccess) return MOEX_ECUDA;
   const int64_t max_ctas = (a.rows + SR - 1) / SR;
   const int grid = static_cast<int>(max_ctas < sm_count() ? max_ctas : sm_count());
-  const int threads = (a.NS * WPS + 1) * 32;
+  const int threads = a.NS * WPS * 32;
   return cuda_status(launch_pdl(kern, dim3(grid), dim3(threads), L.total, s, a));
 }
 
+// Register-staged variant: K <= 2560 (5 slices x 4 warps = 640 threads), the
+// CTA's rows fit NSTG stages, and the columns are few enough that the
+// weights, scales and activations all fit the register budget.
+template <int FMT, int C, int NSTG>
+moex_status launch_reg(const GemvArgs& a, cudaStream_t s) {
+  auto kern = qgemv_reg_kernel<FMT, C, NSTG>;
+  const int64_t cap_rows = static_cast<int64_t>(SR) * NSTG;
+  int64_t grid = sm_count();
+  if ((a.rows + grid - 1) / grid > cap_rows) grid = (a.rows + cap_rows - 1) / cap_rows;
+  if (grid > a.rows) grid = a.rows;
+  const int smem = 4 * NSTG * SR * a.NS * C;
+  if (ensure_smem(reinterpret_cast<const void*>(kern), smem) != cudaSuccess) return MOEX_ECUDA;
+  const int threads = a.NS * REG_WPS * 32;
+  return cuda_status(launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(threads), smem, s, a));
+}
+
+// Consumer layout: for K up to 2560 (<= 5 slices) two warps per slice for
+// <= 4 columns, one for more (register budget of two resident CTAs); for
+// larger K one warp per slice and one CTA per SM.
 template <int FMT, int C>
 moex_status launch_c(const GemvArgs& a, int smem_cap, cudaStream_t s) {
-  switch (warps_per_slice(a.NS)) {
-    case 4: return launch_one<FMT, C, 4>(a, smem_cap, s);
-    case 2: return launch_one<FMT, C, 2>(a, smem_cap, s);
-    default: return launch_one<FMT, C, 1>(a, smem_cap, s);
+  if constexpr (C <= (FMT == MOEX_IQ4_NL ? 4 : 2)) {
+    constexpr int NSTG = FMT == MOEX_IQ4_NL ? 12 : 8;
+    if (a.NS <= 5 && a.rows <= static_cast<int64_t>(sm_count()) * SR * NSTG * 4) return launch_reg<FMT, C, NSTG>(a, s);
   }
+  if (a.NS <= 5) {
+    if constexpr (C <= 4) return launch_one<FMT, C, 2, 2>(a, smem_cap, s);
+    else return launch_one<FMT, C, 1, 2>(a, smem_cap, s);
+  }
+  return launch_one<FMT, C, 1, 1>(a, smem_cap, s);
 }
 
 template <int FMT>
@@ -244,7 +354,7 @@ moex_status launch_qgemv(const moex_qweight* W, const int8_t* xq, const float* x
   a.scrow = static_cast<int>(sc_row_bytes(W->K));
   a.stage_bytes = ((SR * (a.qrow + a.scrow)) + 127) & ~127;
   a.status = device_status_ptr();
-  if (a.NS * warps_per_slice(a.NS) > 15) return MOEX_EUNSUPPORTED;
+  if (a.NS > 16) return MOEX_EUNSUPPORTED;
   const int cap = max_smem_optin();
   for (int c0 = 0; c0 < ncols; c0 += 8) {
     const int C = ncols - c0 < 8 ? ncols - c0 : 8;
