@@ -300,10 +300,10 @@ __device__ __forceinline__ void ring_partials(uint8_t* slot, int nwc, const Cons
   }
 }
 
-// Reduces a lane's partials over its half warp and writes them to
-// red[row][ks][c] (row < nrows).
-template <int C, int WPS, int N>
-__device__ __forceinline__ void reduce_to_red(float (&v)[N], const ConsumerPos& p, int nrows, int NS, float* red) {
+// Reduces a lane's partials over its half warp and hands each (row, c) sum
+// of this slice to out(row, c, value) (row < nrows).
+template <int C, int WPS, int N, typename Out>
+__device__ __forceinline__ void reduce_out(float (&v)[N], const ConsumerPos& p, int nrows, Out&& out) {
   constexpr int RPH = SR / (2 * WPS);
   constexpr int V = RPH * C;
   halving_reduce<N, 8>(v, p.lane);
@@ -315,7 +315,7 @@ __device__ __forceinline__ void reduce_to_red(float (&v)[N], const ConsumerPos& 
       if (idx < V) {
         const int rr = idx / C, c = idx % C;
         const int row = p.jw * 2 + p.hf + 2 * WPS * rr;
-        if (row < nrows) red[(row * NS + p.ks) * C + c] = v[i];
+        if (row < nrows) out(row, c, v[i]);
       }
     }
   } else {
@@ -325,10 +325,16 @@ __device__ __forceinline__ void reduce_to_red(float (&v)[N], const ConsumerPos& 
       if (idx < V) {
         const int rr = idx / C, c = idx % C;
         const int row = p.jw * 2 + p.hf + 2 * WPS * rr;
-        if (row < nrows) red[(row * NS + p.ks) * C + c] = v[0];
+        if (row < nrows) out(row, c, v[0]);
       }
     }
   }
+}
+
+// reduce_out into red[row][ks][c].
+template <int C, int WPS, int N>
+__device__ __forceinline__ void reduce_to_red(float (&v)[N], const ConsumerPos& p, int nrows, int NS, float* red) {
+  reduce_out<C, WPS, N>(v, p, nrows, [&](int row, int c, float val) { red[(row * NS + p.ks) * C + c] = val; });
 }
 
 template <int C, int WPS>
@@ -392,6 +398,80 @@ __device__ __forceinline__ void prefetch_l2(const void* src, int64_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
     p += n;
     bytes -= n;
+  }
+}
+
+// ----------------------------------------------------------------- TMA ring
+
+// A ring of shared-memory stages filled by one producer thread with bulk
+// (TMA) copies of contiguous plane rows: slot = [SR rows x qrow bytes of
+// quants][SR rows x scrow bytes of FP16 scales].  full[slot] completes when a
+// stage's bytes have landed; empty[slot] when every consumer warp has let go.
+struct TmaRing {
+  uint64_t* full;
+  uint64_t* empty;
+  uint8_t* slots;
+  int nst, slot_bytes, qrow, scrow;
+  int slot_rows;  // row capacity of a slot (scales start at slot_rows * qrow)
+  __device__ uint8_t* slot(int it) const { return slots + static_cast<size_t>(it % nst) * slot_bytes; }
+};
+
+// Producer side: waits for the slot of stage `it` to be free, then copies
+// `nrows` rows starting at qsrc / ssrc.  Returns false on timeout / abort.
+__device__ __forceinline__ bool tma_ring_fill(const TmaRing& R, int it, const uint8_t* qsrc, const uint8_t* ssrc,
+                                              int nrows, uint64_t policy, volatile int* abort) {
+  const int s = it % R.nst;
+  if (it >= R.nst && !mbar_wait(&R.empty[s], ((it / R.nst) - 1) & 1, abort)) return false;
+  uint8_t* dst = R.slots + static_cast<size_t>(s) * R.slot_bytes;
+  mbar_arrive_expect_tx(&R.full[s], nrows * (R.qrow + R.scrow));
+  bulk_g2s_stream(dst, qsrc, nrows * R.qrow, &R.full[s], policy);
+  bulk_g2s_stream(dst + R.slot_rows * R.qrow, ssrc, nrows * R.scrow, &R.full[s], policy);
+  return true;
+}
+
+// Consumer side: per-lane partial sums of 8 rows (rows row0 .. row0+nrows-1
+// of the slot of ring stage `it`), after waiting for the slot to land when
+// `wait` is set.  Returns false on timeout / abort.
+template <int FMT, int C, int WPS, int N>
+__device__ __forceinline__ bool tma_ring_partials(const TmaRing& R, int it, const ConsumerPos& p, int nrows, int NB,
+                                                  const ActRegs<FMT, C>& act, float (&v)[N], volatile int* abort,
+                                                  int row0 = 0, bool wait = true) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = 0.f;
+  if (wait && !mbar_wait(&R.full[it % R.nst], (it / R.nst) & 1, abort)) return false;
+  const uint8_t* st = R.slot(it) + row0 * R.qrow;
+  const uint8_t* sc = R.slot(it) + R.slot_rows * R.qrow + row0 * R.scrow;
+  const int b = p.ks * SLICE + p.li;
+  if (b >= NB) return true;
+  constexpr int RPH = SR / (2 * WPS);
+#pragma unroll
+  for (int rr = 0; rr < RPH; ++rr) {
+    const int row = p.jw * 2 + p.hf + 2 * WPS * rr;
+    if (row < nrows) {
+      const uint8_t* wq = st + row * R.qrow + b * FmtTraits<FMT>::QBYTES;
+      const float dw = __half2float(reinterpret_cast<const __half*>(sc + row * R.scrow)[b]);
+      block_row_dots<FMT, C>(wq, dw, act, &v[rr * C]);
+    }
+  }
+  return true;
+}
+
+// Consumer side: this warp is done reading stage `it`'s slot.
+__device__ __forceinline__ void tma_ring_release(const TmaRing& R, int it, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&R.empty[it % R.nst]);
+}
+
+// Sum over the K slices (in slice order) of red[row][ks][c] for rows
+// [row0, row0+nrows), spread over `nthreads` threads starting at `tid`.
+template <int C, typename Out>
+__device__ __forceinline__ void slices_final(const float* red, int row0, int nrows, int NS, int tid, int nthreads,
+                                             Out&& out) {
+  for (int idx = tid; idx < nrows * C; idx += nthreads) {
+    const int row = row0 + idx / C, c = idx % C;
+    float s = red[(row * NS + 0) * C + c];
+    for (int ks = 1; ks < NS; ++ks) s = s + red[(row * NS + ks) * C + c];
+    out(row, c, s);
   }
 }
 

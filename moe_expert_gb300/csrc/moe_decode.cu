@@ -63,34 +63,53 @@ struct Groups {
   int ent[MAX_ENTRIES];
 };
 
-__device__ void build_groups(Groups& G, const int32_t* ids, int n, int E, uint32_t* status) {
-  int m = 0;
-  for (int j = 0; j < n; ++j) {
-    const int e = ids[j];
+// Builds the groups from a shared-memory copy of the ids with every thread
+// of the block (n <= 64): entry j's position in (expert, entry) order is the
+// number of entries before it in that order; a group starts where the expert
+// changes or every MAX_GROUP entries of one expert.  Must be called by all
+// threads; ends with __syncthreads().
+__device__ void build_groups(Groups& G, const int32_t* ids, int n, int E, uint32_t* status, int* scratch) {
+  // scratch: [MAX_ENTRIES] valid-position map
+  const int j = threadIdx.x;
+  int e = -1;
+  if (j < n) {
+    e = ids[j];
     if (e < 0 || e >= E) {
       flag_status(status, DEV_BAD_ROUTE);
-      continue;
-    }
-    // insertion by (expert, entry)
-    int p = m;
-    while (p > 0 && ids[G.ent[p - 1]] > e) {
-      G.ent[p] = G.ent[p - 1];
-      --p;
-    }
-    G.ent[p] = j;
-    ++m;
-  }
-  int ng = 0;
-  for (int p = 0; p < m; ++p) {
-    const int e = ids[G.ent[p]];
-    if (ng == 0 || G.gexp[ng - 1] != e || p - G.gstart[ng - 1] >= MAX_GROUP) {
-      G.gexp[ng] = e;
-      G.gstart[ng] = p;
-      ++ng;
+      e = -1;
     }
   }
-  G.gstart[ng] = m;
-  G.ng = ng;
+  int pos = -1, run = 0;
+  if (e >= 0) {
+    pos = 0;
+    for (int i = 0; i < n; ++i) {
+      const int ei = ids[i];
+      if (ei < 0 || ei >= E) continue;
+      if (ei < e || (ei == e && i < j)) ++pos;
+      if (ei < e) ++run;
+    }
+    G.ent[pos] = j;
+  }
+  // group starts, by position
+  if (j < MAX_ENTRIES) scratch[j] = 0;
+  __syncthreads();
+  if (e >= 0) scratch[pos] = ((pos - run) % MAX_GROUP == 0) ? 1 : 2;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ng = 0, m = 0;
+    for (int p = 0; p < n; ++p) {
+      if (scratch[p] == 0) break;
+      if (scratch[p] == 1) {
+        G.gexp[ng] = ids[G.ent[p]];
+        G.gstart[ng] = p;
+        ++ng;
+      }
+      ++m;
+    }
+    G.gstart[ng] = m;
+    G.ng = ng;
+  }
+  __syncthreads();
 }
 
 // ============================================================== gate / up
@@ -99,15 +118,16 @@ __device__ void build_groups(Groups& G, const int32_t* ids, int n, int E, uint32
 constexpr int NUB = 3;    // unit buffers (SwiGLU inputs of one unit)
 
 struct GuSmem {
-  int cnt, seq, useq, ucnt, abort_flag, groups, xs, xd, red, ubuf, ring, total;
+  int bars, cnt, useq, ucnt, abort_flag, ids, groups, xs, xd, red, ubuf, ring, total;
   __host__ __device__ GuSmem(int T, int H, int NS, int nst, int slot_bytes) {
     const int NB = H / QK;
     int o = 0;
-    cnt = o; o += 4 * NRED;
-    seq = o; o += 4 * NRED;
+    bars = o; o += 16 * nst;
+    cnt = o; o += 4 * nst;
     useq = o; o += 4 * NUB;
     ucnt = o; o += 4 * NUB;
     abort_flag = o; o += 16;
+    ids = o; o += 8 * MAX_ENTRIES;
     o = (o + 15) & ~15;
     groups = o; o += static_cast<int>(sizeof(Groups));
     o = (o + 15) & ~15;
@@ -115,8 +135,8 @@ struct GuSmem {
     o = (o + 15) & ~15;
     xd = o; o += 4 * T * NB;
     o = (o + 15) & ~15;
-    red = o; o += 4 * NRED * SR * NS * MAX_GROUP;
-    ubuf = o; o += 4 * NUB * 64 * MAX_GROUP;
+    red = o; o += 4 * NUB * 64 * NS * MAX_GROUP;   // per unit buffer: [64 rows][NS][C]
+    ubuf = red;
     o = (o + 127) & ~127;
     ring = o; o += nst * slot_bytes;
     total = o;
@@ -126,15 +146,21 @@ struct GuSmem {
 // SwiGLU + q8_1 of one 32-index block of H for C entries, by one warp:
 // lane i takes element i; amax and sum(q) are exact warp reductions, so the
 // block is the same as q8_1_block on the same H values.
+// g and u are first summed over the K slices, in slice order, from the unit
+// buffer ub[row][ks][c] (rows 0..31 gate, 32..63 up).
 template <int C>
 __device__ __forceinline__ void gu_epilogue(const DecodeArgs& a, const Groups& G, int g, int ib, const float* ub,
-                                            int lane) {
+                                            int NS, int lane) {
   const int base = G.gstart[g];
 #pragma unroll
   for (int c = 0; c < C; ++c) {
     const int j = G.ent[base + c];
-    const float gv = ub[lane * MAX_GROUP + c];
-    const float uv = ub[(32 + lane) * MAX_GROUP + c];
+    float gv = ub[(lane * NS + 0) * C + c];
+    float uv = ub[((32 + lane) * NS + 0) * C + c];
+    for (int ks = 1; ks < NS; ++ks) {
+      gv = gv + ub[(lane * NS + ks) * C + c];
+      uv = uv + ub[((32 + lane) * NS + ks) * C + c];
+    }
     const float silu = __fdiv_rn(gv, 1.0f + expf(-gv));
     const float h = __fmul_rn(silu, uv);
     float amax = fabsf(h);
@@ -161,23 +187,32 @@ __device__ __forceinline__ void gu_epilogue(const DecodeArgs& a, const Groups& G
   }
 }
 
-// Shared state of one decode CTA's stage loop.
+// Shared state of one decode CTA's consumer loop.
 struct StageCtx {
-  uint8_t* ring;
-  int slot_bytes, nst, nwc, NS, NB;
+  TmaRing R;
+  int nwc, NS, NB;
   int* cnt;
-  volatile int* seq;
   volatile int* abort_flag;
   float* red;
   uint32_t* status;
 };
 
-// One work unit (group g, intermediate block ib): 8 stages of 8 rows; stage
-// indices it0 .. it0+7.  `issue(it)` refills the ring for any later stage.
-template <int C, int WPS, typename Issue>
-__device__ __forceinline__ void gu_unit(const DecodeArgs& a, const Groups& G, int g, int ib, int ui, int it0,
+__device__ __forceinline__ void ctx_abort(const StageCtx& S, int lane, bool& dead) {
+  if (lane == 0) {
+    *S.abort_flag = 1;
+    flag_status(S.status, DEV_TIMEOUT_PIPE);
+  }
+  dead = true;
+}
+
+// One work unit (group g, intermediate block ib): 8 stages of 8 rows, stage
+// indices ui*8 .. ui*8+7.  Each warp writes its slice's sums of the unit's
+// 64 rows into the unit buffer; the last warp to finish the unit runs the
+// SwiGLU + q8_1 epilogue (no hand-off per stage).
+template <int C, int WPS>
+__device__ __forceinline__ void gu_unit(const DecodeArgs& a, const Groups& G, int g, int ib, int ui,
                                         const StageCtx& S, const ConsumerPos& pos, const int8_t* xs, const float* xd,
-                                        int* ucnt, volatile int* useq, float* ubuf, bool& dead, Issue&& issue) {
+                                        int* ucnt, volatile int* useq, float* ubuf, bool& dead) {
   ActRegs<MOEX_Q8_0, C> act;
   {
     const int8_t* xcol[C];
@@ -192,56 +227,36 @@ __device__ __forceinline__ void gu_unit(const DecodeArgs& a, const Groups& G, in
     load_act<MOEX_Q8_0, C>(act, xcol, dcol, b, b < S.NB, pos.li);
   }
   constexpr int N = Vals<C, WPS>::N;
-  float* ub = ubuf + (ui % NUB) * 64 * MAX_GROUP;
+  float* ub = ubuf + (ui % NUB) * 64 * S.NS * MAX_GROUP;
+  if (!red_slot_wait(&useq[ui % NUB], ui, S.abort_flag)) {
+    ctx_abort(S, pos.lane, dead);
+    return;
+  }
   for (int s = 0; s < 8; ++s) {
-    const int it = it0 + s;
-    cp_async_wait(S.nst - 1);
+    const int it = ui * 8 + s;
     float v[N];
-    if (!dead) ring_partials<MOEX_Q8_0, C, WPS, N>(S.ring + static_cast<size_t>(it % S.nst) * S.slot_bytes, S.nwc, pos,
-                                                   SR, S.NB, act, v);
-    issue(it + S.nst);
-    if (dead) continue;
-    const int rs_slot = it % NRED;
-    if (!red_slot_wait(&S.seq[rs_slot], it, S.abort_flag) || (s == 0 && !red_slot_wait(&useq[ui % NUB], ui, S.abort_flag))) {
-      if (pos.lane == 0) {
-        *S.abort_flag = 1;
-        flag_status(S.status, DEV_TIMEOUT_PIPE);
-      }
-      dead = true;
-      continue;
+    if (!tma_ring_partials<MOEX_Q8_0, C, WPS, N>(S.R, it, pos, SR, S.NB, act, v, S.abort_flag)) {
+      ctx_abort(S, pos.lane, dead);
+      return;
     }
-    float* rs = S.red + rs_slot * (SR * S.NS * MAX_GROUP);
-    reduce_to_red<C, WPS, N>(v, pos, SR, S.NS, rs);
-    if (stage_arrive_last(&S.cnt[rs_slot], S.nwc, pos.lane)) {
-      if (!red_slot_wait(&useq[ui % NUB], ui, S.abort_flag)) {
-        if (pos.lane == 0) {
-          *S.abort_flag = 1;
-          flag_status(S.status, DEV_TIMEOUT_PIPE);
-        }
-        dead = true;
-        continue;
-      }
-      stage_final<C>(rs, SR, S.NS, pos.lane,
-                     [&](int row, int c, float val) { ub[(s * SR + row) * MAX_GROUP + c] = val; });
-      __syncwarp();
-      int old = 0;
-      if (pos.lane == 0) {
-        S.cnt[rs_slot] = 0;
-        __threadfence_block();
-        S.seq[rs_slot] = it + NRED;
-        old = atomicAdd(&ucnt[ui % NUB], 1);
-      }
-      old = __shfl_sync(0xffffffffu, old, 0);
-      if (old == 7) {  // the unit's eighth stage: SwiGLU + q8_1
-        __threadfence_block();
-        gu_epilogue<C>(a, G, g, ib, ub, pos.lane);
-        __syncwarp();
-        if (pos.lane == 0) {
-          ucnt[ui % NUB] = 0;
-          __threadfence_block();
-          useq[ui % NUB] = ui + NUB;
-        }
-      }
+    reduce_to_red<C, WPS, N>(v, pos, SR, S.NS, ub + s * SR * S.NS * C);
+    tma_ring_release(S.R, it, pos.lane);
+  }
+  int old = 0;
+  __syncwarp();
+  if (pos.lane == 0) {
+    __threadfence_block();
+    old = atomicAdd(&ucnt[ui % NUB], 1);
+  }
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old == S.nwc - 1) {  // last warp of the unit: SwiGLU + q8_1
+    __threadfence_block();
+    gu_epilogue<C>(a, G, g, ib, ub, S.NS, pos.lane);
+    __syncwarp();
+    if (pos.lane == 0) {
+      ucnt[ui % NUB] = 0;
+      __threadfence_block();
+      useq[ui % NUB] = ui + NUB;
     }
   }
 }
@@ -249,38 +264,55 @@ __device__ __forceinline__ void gu_unit(const DecodeArgs& a, const Groups& G, in
 template <int WPS, int MAXT>
 __global__ void __launch_bounds__(MAXT, 1) moe_gu_kernel(DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  using R = Ring<MOEX_Q8_0, WPS>;
+  MOEX_TRACE_BEGIN();
   const int NB = a.H / QK;
   const int NS = num_slices(NB);
   const int nwc = NS * WPS;
-  const int slot_bytes = R::slot_bytes(nwc);
-  const GuSmem L(a.T, a.H, NS, a.nst, slot_bytes);
-  int* cnt = reinterpret_cast<int*>(smem + L.cnt);
-  volatile int* seq = reinterpret_cast<volatile int*>(smem + L.seq);
+  const GuSmem L(a.T, a.H, NS, a.nst, a.stage_bytes);
+  StageCtx S;
+  S.R.full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  S.R.empty = S.R.full + a.nst;
+  S.R.slots = smem + L.ring;
+  S.R.nst = a.nst;
+  S.R.slot_bytes = a.stage_bytes;
+  S.R.qrow = a.gu_qrow;
+  S.R.scrow = a.gu_scrow;
+  S.R.slot_rows = SR;
+  S.nwc = nwc;
+  S.NS = NS;
+  S.NB = NB;
+  S.cnt = reinterpret_cast<int*>(smem + L.cnt);
+  S.abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+  S.red = reinterpret_cast<float*>(smem + L.red);
+  S.status = a.status;
   volatile int* useq = reinterpret_cast<volatile int*>(smem + L.useq);
   int* ucnt = reinterpret_cast<int*>(smem + L.ucnt);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+  int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L.ids);
   Groups& G = *reinterpret_cast<Groups*>(smem + L.groups);
   int8_t* xs = reinterpret_cast<int8_t*>(smem + L.xs);
   float* xd = reinterpret_cast<float*>(smem + L.xd);
   float* ubuf = reinterpret_cast<float*>(smem + L.ubuf);
-  uint8_t* ring = smem + L.ring;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const ConsumerPos pos = consumer_pos(warp, lane, WPS);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NRED; ++i) {
-      cnt[i] = 0;
-      seq[i] = i;
+    for (int i = 0; i < a.nst; ++i) {
+      mbar_init(&S.R.full[i], 1);
+      mbar_init(&S.R.empty[i], nwc);
+      S.cnt[i] = 0;
     }
     for (int i = 0; i < NUB; ++i) {
       ucnt[i] = 0;
       useq[i] = i;
     }
-    *abort_flag = 0;
+    *S.abort_flag = 0;
+    fence_mbar_init();
   }
+  MOEX_TRACE_STAMP(0);
   pdl_wait();  // routing ids and the layer input come from earlier kernels
-  if (threadIdx.x == 0) build_groups(G, a.ids, a.n, a.E, a.status);
+  MOEX_TRACE_STAMP(1);
+  for (int j = threadIdx.x; j < a.n; j += blockDim.x) ids_s[j] = a.ids[j];
+  __syncthreads();
+  build_groups(G, ids_s, a.n, a.E, a.status, ids_s + MAX_ENTRIES);
   // q8_1 of the layer input (same block arithmetic as quantize_q8_1)
   for (int t = threadIdx.x; t < a.T * NB; t += blockDim.x) {
     const int tok = t / NB, b = t % NB;
@@ -292,62 +324,54 @@ __global__ void __launch_bounds__(MAXT, 1) moe_gu_kernel(DecodeArgs a) {
       v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
     }
     uint32_t qw[8];
-    float d, s;
-    q8_1_block(v, qw, &d, &s);
+    float d, s_;
+    q8_1_block(v, qw, &d, &s_);
     uint4* dst = reinterpret_cast<uint4*>(xs + tok * a.H + b * QK);
     dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
     dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
     xd[tok * NB + b] = d;
   }
   __syncthreads();
+  MOEX_TRACE_STAMP(2);
   pdl_launch_dependents();  // after the wait: the routing ids are complete
 
   const int ib_per = a.I / QK;
   const int units = G.ng * ib_per;
   const int nunit = units > static_cast<int>(blockIdx.x) ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-  const int nstage = nunit * 8;
-  auto unit_rows = [&](int ui, int s) {
-    const int u = blockIdx.x + ui * gridDim.x;
-    const int g = u / ib_per, ib = u % ib_per;
-    const int64_t mat_row0 = static_cast<int64_t>(G.gexp[g]) * 2 * a.I;
-    return mat_row0 + (s < 4 ? ib * QK + s * SR : a.I + ib * QK + (s - 4) * SR);
-  };
-  auto issue = [&](int it) {
-    if (it < nstage) {
-      const int64_t r0 = unit_rows(it / 8, it % 8);
-      ring_issue<MOEX_Q8_0, WPS>(ring + static_cast<size_t>(it % a.nst) * slot_bytes, nwc, pos,
-                                 a.gu_qs + r0 * a.gu_qrow, a.gu_sc + r0 * a.gu_scrow, SR, a.gu_qrow, a.gu_scrow, NB);
-      // one unit ahead of the ring: ask for the following unit in L2
-      if (it % 8 == 0 && threadIdx.x == 0 && it / 8 + 1 < nunit) {
-        for (int half = 0; half < 2; ++half) {
-          const int64_t p0 = unit_rows(it / 8 + 1, half * 4);
-          prefetch_l2(a.gu_qs + p0 * a.gu_qrow, 32 * static_cast<int64_t>(a.gu_qrow));
-          prefetch_l2(a.gu_sc + p0 * a.gu_scrow, 32 * static_cast<int64_t>(a.gu_scrow));
+
+  if (warp == nwc) {
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      int issued = 0;
+      for (int ui = 0; ui < nunit && !*S.abort_flag; ++ui) {
+        const int u = blockIdx.x + ui * gridDim.x;
+        const int g = u / ib_per, ib = u % ib_per;
+        const int64_t mat_row0 = static_cast<int64_t>(G.gexp[g]) * 2 * a.I;
+        for (int s = 0; s < 8; ++s) {
+          const int it = ui * 8 + s;
+          const int64_t r0 = mat_row0 + (s < 4 ? ib * QK + s * SR : a.I + ib * QK + (s - 4) * SR);
+          if (!tma_ring_fill(S.R, it, a.gu_qs + r0 * a.gu_qrow, a.gu_sc + r0 * a.gu_scrow, SR, pol, S.abort_flag)) {
+            *S.abort_flag = 1;
+            flag_status(a.status, DEV_TIMEOUT_PIPE);
+            break;
+          }
+          issued = it + 1;
         }
       }
+      if (*S.abort_flag)
+        for (int it = max(0, issued - a.nst); it < issued; ++it)
+          mbar_wait(&S.R.full[it % a.nst], (it / a.nst) & 1, nullptr);
     }
-    cp_async_commit();
-  };
-  for (int it = 0; it < a.nst; ++it) issue(it);
+    return;
+  }
 
-  StageCtx S;
-  S.ring = ring;
-  S.slot_bytes = slot_bytes;
-  S.nst = a.nst;
-  S.nwc = nwc;
-  S.NS = NS;
-  S.NB = NB;
-  S.cnt = cnt;
-  S.seq = seq;
-  S.abort_flag = abort_flag;
-  S.red = reinterpret_cast<float*>(smem + L.red);
-  S.status = a.status;
+  const ConsumerPos pos = consumer_pos(warp, lane, WPS);
   bool dead = false;
-  for (int ui = 0; ui < nunit; ++ui) {
+  for (int ui = 0; ui < nunit && !dead; ++ui) {
     const int u = blockIdx.x + ui * gridDim.x;
     const int g = u / ib_per, ib = u % ib_per;
     const int m = G.gstart[g + 1] - G.gstart[g];
-#define MOEX_GU(CC) gu_unit<CC, WPS>(a, G, g, ib, ui, ui * 8, S, pos, xs, xd, ucnt, useq, ubuf, dead, issue)
+#define MOEX_GU(CC) gu_unit<CC, WPS>(a, G, g, ib, ui, S, pos, xs, xd, ucnt, useq, ubuf, dead)
     switch (m) {
       case 1: MOEX_GU(1); break;
       case 2: MOEX_GU(2); break;
@@ -359,20 +383,22 @@ __global__ void __launch_bounds__(MAXT, 1) moe_gu_kernel(DecodeArgs a) {
       default: MOEX_GU(8); break;
     }
 #undef MOEX_GU
+    if (ui == 0) MOEX_TRACE_STAMP(3);
   }
-  cp_async_wait(0);
+  MOEX_TRACE_STAMP(4);
 }
 
 // ============================================================== down + combine
 
 struct DnSmem {
-  int cnt, seq, abort_flag, groups, hs, hd, red, osum, ring, total;
+  int bars, cnt, abort_flag, ids, groups, hs, hd, red, osum, ring, total;
   __host__ __device__ DnSmem(int n, int I, int NS, int rows_max, int nst, int slot_bytes) {
     const int NB = I / QK;
     int o = 0;
-    cnt = o; o += 4 * NRED;
-    seq = o; o += 4 * NRED;
+    bars = o; o += 16 * nst;
+    cnt = o; o += 4 * nst;
     abort_flag = o; o += 16;
+    ids = o; o += 8 * MAX_ENTRIES;
     o = (o + 15) & ~15;
     groups = o; o += static_cast<int>(sizeof(Groups));
     o = (o + 15) & ~15;
@@ -380,8 +406,8 @@ struct DnSmem {
     o = (o + 15) & ~15;
     hd = o; o += 4 * n * NB;
     o = (o + 15) & ~15;
-    red = o; o += 4 * NRED * SR * NS * MAX_GROUP;
-    osum = o; o += 4 * n * rows_max;
+    red = o; o += 4 * n * rows_max * NS;   // [entry][row][ks]
+    osum = red;
     o = (o + 127) & ~127;
     ring = o; o += nst * slot_bytes;
     total = o;
@@ -392,10 +418,10 @@ struct DnSmem {
 // of balanced size; stage s covers rows [s*nrows/ns, (s+1)*nrows/ns).
 __device__ __forceinline__ int dn_nstages(int nrows) { return (nrows + SR - 1) / SR; }
 
-template <int FMT, int C, int WPS, typename Issue>
+template <int FMT, int C, int WPS>
 __device__ __forceinline__ void dn_group(const DecodeArgs& a, const Groups& G, int g, int it0, int nrows,
                                          const StageCtx& S, const ConsumerPos& pos, const int8_t* hs, const float* hd,
-                                         float* osum, int rows_max, bool& dead, Issue&& issue) {
+                                         float* dred, int rows_max, bool& dead) {
   ActRegs<FMT, C> act;
   {
     const int8_t* xcol[C];
@@ -410,104 +436,99 @@ __device__ __forceinline__ void dn_group(const DecodeArgs& a, const Groups& G, i
     load_act<FMT, C>(act, xcol, dcol, b, b < S.NB, pos.li);
   }
   constexpr int N = Vals<C, WPS>::N;
-  const int ns = dn_nstages(nrows);
-  for (int s = 0; s < ns; ++s) {
-    const int it = it0 + s;
-    const int rlo = s * nrows / ns, rhi = (s + 1) * nrows / ns;
-    cp_async_wait(S.nst - 1);
+  const int gbase = G.gstart[g];
+  // the group's rows arrive as one ring slot; computed 8 rows at a time
+  for (int rlo = 0; rlo < nrows; rlo += SR) {
+    const int n = nrows - rlo < SR ? nrows - rlo : SR;
     float v[N];
-    if (!dead) ring_partials<FMT, C, WPS, N>(S.ring + static_cast<size_t>(it % S.nst) * S.slot_bytes, S.nwc, pos,
-                                             rhi - rlo, S.NB, act, v);
-    issue(it + S.nst);
-    if (dead) continue;
-    const int rs_slot = it % NRED;
-    if (!red_slot_wait(&S.seq[rs_slot], it, S.abort_flag)) {
-      if (pos.lane == 0) {
-        *S.abort_flag = 1;
-        flag_status(S.status, DEV_TIMEOUT_PIPE);
-      }
-      dead = true;
-      continue;
+    if (!tma_ring_partials<FMT, C, WPS, N>(S.R, it0, pos, n, S.NB, act, v, S.abort_flag, rlo, rlo == 0)) {
+      ctx_abort(S, pos.lane, dead);
+      return;
     }
-    float* rs = S.red + rs_slot * (SR * S.NS * MAX_GROUP);
-    reduce_to_red<C, WPS, N>(v, pos, rhi - rlo, S.NS, rs);
-    if (stage_arrive_last(&S.cnt[rs_slot], S.nwc, pos.lane)) {
-      const int gbase = G.gstart[g];
-      stage_final<C>(rs, rhi - rlo, S.NS, pos.lane, [&](int row, int c, float val) {
-        osum[G.ent[gbase + c] * rows_max + rlo + row] = val;
-      });
-      __syncwarp();
-      if (pos.lane == 0) {
-        S.cnt[rs_slot] = 0;
-        __threadfence_block();
-        S.seq[rs_slot] = it + NRED;
-      }
-    }
+    reduce_out<C, WPS, N>(v, pos, n, [&](int row, int c, float val) {
+      dred[(G.ent[gbase + c] * rows_max + rlo + row) * S.NS + pos.ks] = val;
+    });
   }
+  tma_ring_release(S.R, it0, pos.lane);
 }
 
 template <int FMT, int WPS, int MAXT>
 __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  using R = Ring<FMT, WPS>;
+  MOEX_TRACE_BEGIN();
   const int NB = a.I / QK;
   const int NS = num_slices(NB);
   const int nwc = NS * WPS;
-  const int slot_bytes = R::slot_bytes(nwc);
   const int G_ = gridDim.x;
   const int rows_max = (a.H + G_ - 1) / G_;
-  const DnSmem L(a.n, a.I, NS, rows_max, a.nst, slot_bytes);
-  int* cnt = reinterpret_cast<int*>(smem + L.cnt);
-  volatile int* seq = reinterpret_cast<volatile int*>(smem + L.seq);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+  const DnSmem L(a.n, a.I, NS, rows_max, a.nst, a.stage_bytes);
+  StageCtx S;
+  S.R.full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  S.R.empty = S.R.full + a.nst;
+  S.R.slots = smem + L.ring;
+  S.R.nst = a.nst;
+  S.R.slot_bytes = a.stage_bytes;
+  S.R.qrow = a.dn_qrow;
+  S.R.scrow = a.dn_scrow;
+  S.R.slot_rows = rows_max;
+  S.nwc = nwc;
+  S.NS = NS;
+  S.NB = NB;
+  S.cnt = reinterpret_cast<int*>(smem + L.cnt);
+  S.abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+  S.red = reinterpret_cast<float*>(smem + L.red);
+  S.status = a.status;
+  int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L.ids);
   Groups& G = *reinterpret_cast<Groups*>(smem + L.groups);
   int8_t* hs = reinterpret_cast<int8_t*>(smem + L.hs);
   float* hd = reinterpret_cast<float*>(smem + L.hd);
   float* osum = reinterpret_cast<float*>(smem + L.osum);
-  uint8_t* ring = smem + L.ring;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const ConsumerPos pos = consumer_pos(warp, lane, WPS);
   const int row_begin = static_cast<int>(static_cast<int64_t>(a.H) * blockIdx.x / G_);
   const int row_end = static_cast<int>(static_cast<int64_t>(a.H) * (blockIdx.x + 1) / G_);
   const int nrows = row_end - row_begin;
   const int ns = dn_nstages(nrows);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NRED; ++i) {
-      cnt[i] = 0;
-      seq[i] = i;
+    for (int i = 0; i < a.nst; ++i) {
+      mbar_init(&S.R.full[i], 1);
+      mbar_init(&S.R.empty[i], nwc);
+      S.cnt[i] = 0;
     }
-    *abort_flag = 0;
-    // The routing ids were complete before the gate/up kernel let this grid
-    // launch, so they are read before griddepcontrol.wait.
-    build_groups(G, a.ids, a.n, a.E, nullptr);
+    *S.abort_flag = 0;
+    fence_mbar_init();
   }
+  // The routing ids were complete before the gate/up kernel let this grid
+  // launch, so they are read before griddepcontrol.wait.
+  for (int j = threadIdx.x; j < a.n; j += blockDim.x) ids_s[j] = a.ids[j];
   __syncthreads();
-  const int nstage = G.ng * ns;
-  if (threadIdx.x == 0) {
-    // the CTA's whole share of the routed experts' rows into L2
-    for (int g = 0; g < G.ng; ++g) {
-      const int64_t r0 = static_cast<int64_t>(G.gexp[g]) * a.H + row_begin;
-      prefetch_l2(a.dn_qs + r0 * a.dn_qrow, static_cast<int64_t>(nrows) * a.dn_qrow);
-      prefetch_l2(a.dn_sc + r0 * a.dn_scrow, static_cast<int64_t>(nrows) * a.dn_scrow);
-    }
-  }
-  auto issue = [&](int it) {
-    if (it < nstage) {
-      const int g = it / ns, s = it % ns;
-      const int rlo = s * nrows / ns, rhi = (s + 1) * nrows / ns;
-      const int64_t r0 = static_cast<int64_t>(G.gexp[g]) * a.H + row_begin + rlo;
-      ring_issue<FMT, WPS>(ring + static_cast<size_t>(it % a.nst) * slot_bytes, nwc, pos, a.dn_qs + r0 * a.dn_qrow,
-                           a.dn_sc + r0 * a.dn_scrow, rhi - rlo, a.dn_qrow, a.dn_scrow, NB);
-    }
-    cp_async_commit();
-  };
-  for (int it = 0; it < a.nst; ++it) issue(it);
+  build_groups(G, ids_s, a.n, a.E, nullptr, ids_s + MAX_ENTRIES);
+  MOEX_TRACE_STAMP(0);
   pdl_launch_dependents();
 
-  // Hq of every entry into shared memory, after the gate/up grid
+  if (warp == nwc) {
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      int issued = 0;
+      for (int g = 0; g < G.ng; ++g) {
+        const int64_t r0 = static_cast<int64_t>(G.gexp[g]) * a.H + row_begin;
+        if (!tma_ring_fill(S.R, g, a.dn_qs + r0 * a.dn_qrow, a.dn_sc + r0 * a.dn_scrow, nrows, pol, S.abort_flag)) {
+          *S.abort_flag = 1;
+          flag_status(a.status, DEV_TIMEOUT_PIPE);
+          break;
+        }
+        issued = g + 1;
+      }
+      if (*S.abort_flag)
+        for (int i = max(0, issued - a.nst); i < issued; ++i) mbar_wait(&S.R.full[i % a.nst], (i / a.nst) & 1, nullptr);
+    }
+    return;
+  }
+
+  // consumers: Hq of every entry into shared memory, after the gate/up grid
   pdl_wait();
+  MOEX_TRACE_STAMP(1);
   const int nthr = nwc * 32;
   {
     const int4* src = reinterpret_cast<const int4*>(a.hq);
@@ -515,25 +536,14 @@ __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
     for (int i = threadIdx.x; i < a.n * a.I / 16; i += nthr) dst[i] = src[i];
     const float2* dsrc = reinterpret_cast<const float2*>(a.hds);
     for (int i = threadIdx.x; i < a.n * NB; i += nthr) hd[i] = dsrc[i].x;
-    for (int i = threadIdx.x; i < a.n * rows_max; i += nthr) osum[i] = 0.f;
-    __syncthreads();
+    for (int i = threadIdx.x; i < a.n * rows_max * NS; i += nthr) osum[i] = 0.f;
+    named_bar_sync(1, nthr);
   }
-  StageCtx S;
-  S.ring = ring;
-  S.slot_bytes = slot_bytes;
-  S.nst = a.nst;
-  S.nwc = nwc;
-  S.NS = NS;
-  S.NB = NB;
-  S.cnt = cnt;
-  S.seq = seq;
-  S.abort_flag = abort_flag;
-  S.red = reinterpret_cast<float*>(smem + L.red);
-  S.status = a.status;
+  const ConsumerPos pos = consumer_pos(warp, lane, WPS);
   bool dead = false;
-  for (int g = 0; g < G.ng; ++g) {
+  for (int g = 0; g < G.ng && !dead; ++g) {
     const int m = G.gstart[g + 1] - G.gstart[g];
-#define MOEX_DN(CC) dn_group<FMT, CC, WPS>(a, G, g, g * ns, nrows, S, pos, hs, hd, osum, rows_max, dead, issue)
+#define MOEX_DN(CC) dn_group<FMT, CC, WPS>(a, G, g, g, nrows, S, pos, hs, hd, osum, rows_max, dead)
     switch (m) {
       case 1: MOEX_DN(1); break;
       case 2: MOEX_DN(2); break;
@@ -545,21 +555,26 @@ __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
       default: MOEX_DN(8); break;
     }
 #undef MOEX_DN
+    if (g == 0) MOEX_TRACE_STAMP(2);
   }
-  cp_async_wait(0);
-  __syncthreads();
+  MOEX_TRACE_STAMP(3);
+  named_bar_sync(1, nthr);
   // combine: out[t][r] = sum over slots in order of w[t,slot] * o[(t,slot)][r]
   for (int i = threadIdx.x; i < a.T * nrows; i += nthr) {
     const int t = i / nrows, rl = i % nrows;
     float acc = 0.f;
     for (int s = 0; s < a.k; ++s) {
       const int j = t * a.k + s;
-      const int e = a.ids[j];
+      const int e = ids_s[j];
       if (e < 0 || e >= a.E) continue;
-      acc = __fadd_rn(acc, __fmul_rn(a.w[j], osum[j * rows_max + rl]));
+      const float* pr = osum + (j * rows_max + rl) * NS;
+      float o = pr[0];
+      for (int ks = 1; ks < NS; ++ks) o = o + pr[ks];   // slice order, as the dense GEMV
+      acc = __fadd_rn(acc, __fmul_rn(a.w[j], o));
     }
     a.out[static_cast<int64_t>(t) * a.H + row_begin + rl] = acc;
   }
+  MOEX_TRACE_STAMP(4);
 }
 
 // ============================================================== host side
@@ -577,8 +592,9 @@ template <int WPS, int MAXT>
 moex_status launch_gu(const DecodeArgs& base, int smem_cap, cudaStream_t s) {
   DecodeArgs a = base;
   const int NB = a.H / QK, NS = num_slices(NB);
-  const int slot_bytes = Ring<MOEX_Q8_0, WPS>::slot_bytes(NS * WPS);
-  int nst = 8;
+  const int slot_bytes = ((SR * (a.gu_qrow + a.gu_scrow)) + 127) & ~127;
+  a.stage_bytes = slot_bytes;
+  int nst = 16;
   for (; nst >= 2; --nst)
     if (GuSmem(a.T, a.H, NS, nst, slot_bytes).total <= smem_cap) break;
   if (nst < 2) return MOEX_EUNSUPPORTED;
@@ -589,7 +605,7 @@ moex_status launch_gu(const DecodeArgs& base, int smem_cap, cudaStream_t s) {
   // grid: enough CTAs for the largest possible unit count is not known on
   // the host (it depends on the routing); use every SM.
   const int grid = sm_count();
-  const int threads = NS * WPS * 32;
+  const int threads = (NS * WPS + 1) * 32;
   return cuda_status(launch_pdl(kern, dim3(grid), dim3(threads), L.total, s, a));
 }
 
@@ -597,10 +613,11 @@ template <int FMT, int WPS, int MAXT>
 moex_status launch_dn(const DecodeArgs& base, int smem_cap, cudaStream_t s) {
   DecodeArgs a = base;
   const int NB = a.I / QK, NS = num_slices(NB);
-  const int slot_bytes = Ring<FMT, WPS>::slot_bytes(NS * WPS);
   const int grid = a.H < sm_count() ? a.H : sm_count();
   const int rows_max = (a.H + grid - 1) / grid;
-  int nst = 8;
+  const int slot_bytes = ((rows_max * (a.dn_qrow + a.dn_scrow)) + 127) & ~127;
+  a.stage_bytes = slot_bytes;
+  int nst = 16;
   for (; nst >= 2; --nst)
     if (DnSmem(a.n, a.I, NS, rows_max, nst, slot_bytes).total <= smem_cap) break;
   if (nst < 2) return MOEX_EUNSUPPORTED;
@@ -608,19 +625,20 @@ moex_status launch_dn(const DecodeArgs& base, int smem_cap, cudaStream_t s) {
   const DnSmem L(a.n, a.I, NS, rows_max, nst, slot_bytes);
   auto kern = moe_dn_kernel<FMT, WPS, MAXT>;
   if (ensure_smem(reinterpret_cast<const void*>(kern), L.total) != cudaSuccess) return MOEX_ECUDA;
-  const int threads = NS * WPS * 32;
+  const int threads = (NS * WPS + 1) * 32;
   return cuda_status(launch_pdl(kern, dim3(grid), dim3(threads), L.total, s, a));
 }
 
 // Decode kernels: two warps per K slice up to 8 slices (K <= 4096), else one.
-inline int decode_wps(int NS) { return NS <= 8 ? 2 : 1; }
+inline int decode_wps(int NS) { return NS <= 3 ? 4 : (NS <= 7 ? 2 : 1); }
 
 template <int FMT>
 moex_status launch_dn_fmt(const DecodeArgs& a, int cap, cudaStream_t s) {
   const int NS = num_slices(a.I / QK);
   const int wps = decode_wps(NS);
-  if (wps == 2) return NS * 2 * 32 <= 320 ? launch_dn<FMT, 2, 320>(a, cap, s) : launch_dn<FMT, 2, 512>(a, cap, s);
-  return NS * 32 <= 320 ? launch_dn<FMT, 1, 320>(a, cap, s) : launch_dn<FMT, 1, 512>(a, cap, s);
+  if (wps == 4) return launch_dn<FMT, 4, 416>(a, cap, s);
+  if (wps == 2) return (NS * 2 + 1) * 32 <= 352 ? launch_dn<FMT, 2, 352>(a, cap, s) : launch_dn<FMT, 2, 544>(a, cap, s);
+  return (NS + 1) * 32 <= 352 ? launch_dn<FMT, 1, 352>(a, cap, s) : launch_dn<FMT, 1, 544>(a, cap, s);
 }
 
 }  // namespace
@@ -659,10 +677,12 @@ moex_status launch_moe_decode(const moex_qweight* gu, const moex_qweight* dn, co
   const int NSg = num_slices(a.H / QK), NSd = num_slices(a.I / QK);
   if (NSg > 16 || NSd > 16) return MOEX_EUNSUPPORTED;
   moex_status st;
-  if (decode_wps(NSg) == 2)
-    st = NSg * 64 <= 320 ? launch_gu<2, 320>(a, cap, s) : launch_gu<2, 512>(a, cap, s);
+  if (decode_wps(NSg) == 4)
+    st = launch_gu<4, 416>(a, cap, s);
+  else if (decode_wps(NSg) == 2)
+    st = (NSg * 2 + 1) * 32 <= 352 ? launch_gu<2, 352>(a, cap, s) : launch_gu<2, 544>(a, cap, s);
   else
-    st = NSg * 32 <= 320 ? launch_gu<1, 320>(a, cap, s) : launch_gu<1, 512>(a, cap, s);
+    st = (NSg + 1) * 32 <= 352 ? launch_gu<1, 352>(a, cap, s) : launch_gu<1, 544>(a, cap, s);
   if (st != MOEX_OK) return st;
   return dn->fmt == MOEX_Q8_0 ? launch_dn_fmt<MOEX_Q8_0>(a, cap, s) : launch_dn_fmt<MOEX_IQ4_NL>(a, cap, s);
 }

@@ -17,7 +17,7 @@ struct GemvArgs {
   int K, NB, NS;        // inputs, blocks, K slices
   int qrow, scrow;      // plane row strides (bytes)
   int nst;              // ring slots
-  int stage_bytes;      // unused
+  int stage_bytes;      // bytes of one ring slot
   const int8_t* xq;     // q8_1 quants [ncols][K]
   const float* xds;     // {d, s} [ncols][NB]
   float* y;
@@ -27,55 +27,63 @@ struct GemvArgs {
 
 
 
-// Shared-memory carve-up of the dense GEMV.
+constexpr int GEMV_CHUNK = 8;  // stages whose slice partials are summed together
+
+// Shared-memory carve-up of the dense ring GEMV.
 struct GemvSmem {
-  int cnt, seq, abort_flag, red, ring, total;
+  int bars, cnt, abort_flag, red, ring, total;
   __host__ __device__ GemvSmem(int C, int NS, int nst, int slot_bytes) {
     int o = 0;
-    cnt = o; o += 4 * NRED;
-    seq = o; o += 4 * NRED;
+    bars = o; o += 16 * nst;
+    cnt = o; o += 4 * nst;
     abort_flag = o; o += 16;
     o = (o + 15) & ~15;
-    red = o; o += 4 * NRED * SR * NS * C;
+    red = o; o += 4 * GEMV_CHUNK * SR * NS * C;
     o = (o + 127) & ~127;
     ring = o; o += nst * slot_bytes;
     total = o;
   }
 };
 
-// Threads of a dense GEMV CTA: NS*WPS warps.  MINB == 2 variants keep
-// registers and shared memory small enough that a CTA of the next GEMV in the
-// stream is resident beside this one, so with programmatic dependent launch
-// its weight stream starts while this one drains.
+// Threads of a dense ring GEMV CTA: NS*WPS consumer warps + 1 producer warp.
+// MINB == 2 variants keep registers and shared memory small enough that a
+// CTA of the next GEMV in the stream can be resident beside this one, so
+// with programmatic dependent launch its weight stream starts while this
+// one drains.
 template <int WPS, int MINB>
 struct GemvBounds {
-  static constexpr int MAXT = MINB == 2 ? 5 * WPS * 32 : 512;
+  static constexpr int MAXT = MINB == 2 ? (5 * WPS + 1) * 32 : 512;
 };
 
-// Every CTA owns a contiguous range of rows.  At entry one thread asks for
-// the whole range in L2 (cp.async.bulk.prefetch.L2) and every lane issues
-// its cp.async copies for the first `nst` stages; all of that happens before
-// griddepcontrol.wait, since the weights do not depend on the previous
-// kernel.  Then the activation blocks are loaded straight into registers and
-// the stages are consumed in order, each slot refilled as soon as its lane
-// has read it.  The partial sums of a stage are reduced over the half warp,
-// then over the K slices by the last warp to finish the stage.
+// Ring variant: every CTA owns a contiguous range of rows; one producer
+// thread streams them through a shared-memory ring with bulk (TMA) copies,
+// starting before griddepcontrol.wait (the weights do not depend on the
+// previous kernel); the consumer warps load their activation blocks straight
+// into registers after the wait.  The partial sums of a stage are reduced
+// over the half warp into a per-chunk buffer; every GEMV_CHUNK stages the
+// consumers meet at a barrier and sum over the K slices (no per-stage
+// hand-off between warps).
 template <int FMT, int C, int WPS, int MINB>
 __global__ void __launch_bounds__(GemvBounds<WPS, MINB>::MAXT, MINB) qgemv_kernel(GemvArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   MOEX_TRACE_BEGIN();
-  using R = Ring<FMT, WPS>;
   const int nwc = a.NS * WPS;
-  const int slot_bytes = R::slot_bytes(nwc);
+  const int slot_bytes = a.stage_bytes;
   const GemvSmem L(C, a.NS, a.nst, slot_bytes);
+  TmaRing R;
+  R.full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  R.empty = R.full + a.nst;
+  R.slots = smem + L.ring;
+  R.nst = a.nst;
+  R.slot_bytes = slot_bytes;
+  R.qrow = a.qrow;
+  R.scrow = a.scrow;
+  R.slot_rows = SR;
   int* cnt = reinterpret_cast<int*>(smem + L.cnt);
-  volatile int* seq = reinterpret_cast<volatile int*>(smem + L.seq);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
   float* red = reinterpret_cast<float*>(smem + L.red);
-  uint8_t* ring = smem + L.ring;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const ConsumerPos pos = consumer_pos(warp, lane, WPS);
   const int64_t G = gridDim.x;
   const int64_t row_begin = a.rows * blockIdx.x / G;
   const int64_t row_end = a.rows * (blockIdx.x + 1) / G;
@@ -84,34 +92,43 @@ __global__ void __launch_bounds__(GemvBounds<WPS, MINB>::MAXT, MINB) qgemv_kerne
     const int64_t r0 = row_begin + static_cast<int64_t>(it) * SR;
     return static_cast<int>((row_end - r0) < SR ? (row_end - r0) : SR);
   };
-  auto issue = [&](int it) {
-    if (it < nstage) {
-      const int64_t r0 = row_begin + static_cast<int64_t>(it) * SR;
-      ring_issue<FMT, WPS>(ring + static_cast<size_t>(it % a.nst) * slot_bytes, nwc, pos, a.qs + r0 * a.qrow,
-                           a.sc + r0 * a.scrow, stage_rows(it), a.qrow, a.scrow, a.NB);
-    }
-    cp_async_commit();
-  };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NRED; ++i) {
+    for (int i = 0; i < a.nst; ++i) {
+      mbar_init(&R.full[i], 1);
+      mbar_init(&R.empty[i], nwc);
       cnt[i] = 0;
-      seq[i] = i;
     }
     *abort_flag = 0;
+    fence_mbar_init();
   }
   __syncthreads();
   MOEX_TRACE_STAMP(0);
-  for (int it = 0; it < a.nst; ++it) issue(it);
-  // the stages beyond the ring: into L2 now, before waiting for the previous kernel
-  for (int it = a.nst; it < nstage; ++it) {
-    const int64_t r0 = row_begin + static_cast<int64_t>(it) * SR;
-    lane_prefetch_l2<FMT, WPS>(pos, a.qs + r0 * a.qrow, a.sc + r0 * a.scrow, stage_rows(it), a.qrow, a.scrow, a.NB);
-  }
-  MOEX_TRACE_STAMP(1);
   pdl_launch_dependents();
+
+  if (warp == nwc) {
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      int issued = 0;
+      for (int it = 0; it < nstage; ++it) {
+        const int64_t r0 = row_begin + static_cast<int64_t>(it) * SR;
+        if (!tma_ring_fill(R, it, a.qs + r0 * a.qrow, a.sc + r0 * a.scrow, stage_rows(it), pol, abort_flag)) {
+          *abort_flag = 1;
+          flag_status(a.status, DEV_TIMEOUT_PIPE);
+          break;
+        }
+        issued = it + 1;
+      }
+      // On abort, wait (bounded) for copies still landing in this CTA's smem.
+      if (*abort_flag)
+        for (int it = max(0, issued - a.nst); it < issued; ++it) mbar_wait(&R.full[it % a.nst], (it / a.nst) & 1, nullptr);
+    }
+    return;
+  }
+
+  const ConsumerPos pos = consumer_pos(warp, lane, WPS);
   pdl_wait();  // activations come from the previous kernel
-  MOEX_TRACE_STAMP(2);
+  MOEX_TRACE_STAMP(1);
   ActRegs<FMT, C> act;
   {
     const int8_t* xcol[C];
@@ -124,41 +141,38 @@ __global__ void __launch_bounds__(GemvBounds<WPS, MINB>::MAXT, MINB) qgemv_kerne
     const int b = pos.ks * SLICE + pos.li;
     load_act<FMT, C>(act, xcol, dcol, b, b < a.NB, pos.li, 2);
   }
-  MOEX_TRACE_STAMP(3);
-
   constexpr int N = Vals<C, WPS>::N;
-  for (int it = 0; it < nstage; ++it) {
-    const int n = stage_rows(it);
-    cp_async_wait(a.nst - 1);
-    if (it == 0) MOEX_TRACE_STAMP(4);
-    float v[N];
-    ring_partials<FMT, C, WPS, N>(ring + static_cast<size_t>(it % a.nst) * slot_bytes, nwc, pos, n, a.NB, act, v);
-    issue(it + a.nst);
-    const int rs_slot = it % NRED;
-    if (!red_slot_wait(&seq[rs_slot], it, abort_flag)) {
-      if (lane == 0) {
-        *abort_flag = 1;
-        flag_status(a.status, DEV_TIMEOUT_PIPE);
+  const int nthr = nwc * 32;
+  bool dead = false;
+  for (int c0 = 0; c0 < nstage; c0 += GEMV_CHUNK) {
+    const int c1 = min(c0 + GEMV_CHUNK, nstage);
+    for (int it = c0; it < c1 && !dead; ++it) {
+      const int n = stage_rows(it);
+      float v[N];
+      if (!tma_ring_partials<FMT, C, WPS, N>(R, it, pos, n, a.NB, act, v, abort_flag)) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          flag_status(a.status, DEV_TIMEOUT_PIPE);
+        }
+        dead = true;
+        break;
       }
-      break;
+      reduce_to_red<C, WPS, N>(v, pos, n, a.NS, red + (it - c0) * (SR * a.NS * C));
+      tma_ring_release(R, it, lane);
     }
-    float* rs = red + rs_slot * (SR * a.NS * C);
-    reduce_to_red<C, WPS, N>(v, pos, n, a.NS, rs);
-    if (stage_arrive_last(&cnt[rs_slot], nwc, lane)) {
-      const int64_t r0 = row_begin + static_cast<int64_t>(it) * SR;
+    named_bar_sync(1, nthr);
+    if (!dead) {
+      const int64_t r0 = row_begin + static_cast<int64_t>(c0) * SR;
+      const int64_t span = static_cast<int64_t>(c1 - c0) * SR;
+      const int nrows = static_cast<int>(span < row_end - r0 ? span : row_end - r0);
       float* y = a.y;
       const int64_t ldy = a.ldy;
-      stage_final<C>(rs, n, a.NS, lane, [&](int row, int c, float val) { y[c * ldy + r0 + row] = val; });
-      __syncwarp();
-      if (lane == 0) {
-        cnt[rs_slot] = 0;
-        __threadfence_block();
-        seq[rs_slot] = it + NRED;
-      }
+      slices_final<C>(red, 0, nrows, a.NS, threadIdx.x, nthr,
+                      [&](int row, int c, float val) { y[c * ldy + r0 + row] = val; });
     }
+    named_bar_sync(1, nthr);
   }
-  MOEX_TRACE_STAMP(5);
-  cp_async_wait(0);
+  MOEX_TRACE_STAMP(2);
 }
 
 // ----------------------------------------------------------------- register-staged GEMV
@@ -175,7 +189,6 @@ constexpr int REG_WPS = 4;
 template <int FMT, int C, int NSTG>
 __global__ void __launch_bounds__(640, 1) qgemv_reg_kernel(GemvArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  using R = Ring<FMT, REG_WPS>;  // geometry only: R::QB, R::NCH
   float* red = reinterpret_cast<float*>(smem);  // [NSTG*8 rows][NS][C]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ConsumerPos pos = consumer_pos(warp, lane, REG_WPS);
@@ -187,15 +200,15 @@ __global__ void __launch_bounds__(640, 1) qgemv_reg_kernel(GemvArgs a) {
   const bool bvalid = b < a.NB;
   const int my_row0 = pos.jw * 2 + pos.hf;  // row within each stage
 
-  uint4 q[NSTG][R::NCH];
+  uint4 q[NSTG][FmtTraits<FMT>::QBYTES / 16];
   uint32_t sw[NSTG];
 #pragma unroll
   for (int st = 0; st < NSTG; ++st) {
     const int row = st * SR + my_row0;
     if (bvalid && row < nrows) {
-      const uint8_t* src = a.qs + (row_begin + row) * a.qrow + b * R::QB;
+      const uint8_t* src = a.qs + (row_begin + row) * a.qrow + b * FmtTraits<FMT>::QBYTES;
 #pragma unroll
-      for (int h = 0; h < R::NCH; ++h)
+      for (int h = 0; h < FmtTraits<FMT>::QBYTES / 16; ++h)
         asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(q[st][h].x), "=r"(q[st][h].y), "=r"(q[st][h].z), "=r"(q[st][h].w)
                      : "l"(src + 16 * h));
@@ -204,7 +217,7 @@ __global__ void __launch_bounds__(640, 1) qgemv_reg_kernel(GemvArgs a) {
                    : "l"(a.sc + (row_begin + row) * a.scrow + 4 * (b >> 1)));
     } else {
 #pragma unroll
-      for (int h = 0; h < R::NCH; ++h) q[st][h] = make_uint4(0, 0, 0, 0);
+      for (int h = 0; h < FmtTraits<FMT>::QBYTES / 16; ++h) q[st][h] = make_uint4(0, 0, 0, 0);
       sw[st] = 0;
     }
   }
@@ -230,7 +243,7 @@ __global__ void __launch_bounds__(640, 1) qgemv_reg_kernel(GemvArgs a) {
     for (int i = 0; i < N; ++i) v[i] = 0.f;
     if (bvalid && row < nrows) {
       const uint16_t hb = static_cast<uint16_t>((b & 1) ? (sw[st] >> 16) : (sw[st] & 0xFFFFu));
-      block_dots_from<FMT, C>(q[st][0], q[st][R::NCH - 1], __half2float(__ushort_as_half(hb)), act, v);
+      block_dots_from<FMT, C>(q[st][0], q[st][FmtTraits<FMT>::QBYTES / 16 - 1], __half2float(__ushort_as_half(hb)), act, v);
     }
     halving_reduce<N, 8>(v, lane);
     // lane li holds value li / (16/N) (N < 16 always here)
@@ -279,7 +292,8 @@ moex_status launch_one(const GemvArgs& base, int smem_cap, cudaStream_t s) {
   auto kern = qgemv_kernel<FMT, C, WPS, MINB>;
   // ring slots: as many as fit the budget (two CTAs per SM for MINB == 2), at most 8
   const int budget = MINB == 2 ? 110 * 1024 : smem_cap;
-  const int slot_bytes = Ring<FMT, WPS>::slot_bytes(a.NS * WPS);
+  const int slot_bytes = ((SR * (a.qrow + a.scrow)) + 127) & ~127;
+  a.stage_bytes = slot_bytes;
   int nst = 8;
   for (; nst >= 2; --nst)
     if (GemvSmem(C, a.NS, nst, slot_bytes).total <= budget) break;
@@ -289,7 +303,7 @@ moex_status launch_one(const GemvArgs& base, int smem_cap, cudaStream_t s) {
   if (ensure_smem(reinterpret_cast<const void*>(kern), L.total) != cudaSuccess) return MOEX_ECUDA;
   const int64_t max_ctas = (a.rows + SR - 1) / SR;
   const int grid = static_cast<int>(max_ctas < sm_count() ? max_ctas : sm_count());
-  const int threads = a.NS * WPS * 32;
+  const int threads = (a.NS * WPS + 1) * 32;
   return cuda_status(launch_pdl(kern, dim3(grid), dim3(threads), L.total, s, a));
 }
 
