@@ -182,6 +182,40 @@ moex_status moex_moe_decode_debug(const moex_qweight* gate_up, const moex_qweigh
                                   size_t ws_bytes, float* gu_dbg, float* h_dbg, int8_t* hq_dbg, float* hds_dbg,
                                   moex_stream stream);
 
+/* Workspace bytes of moex_moe_prefill for T tokens, top-k, E experts. */
+size_t moex_moe_prefill_workspace_bytes(int T, int k, int E, int64_t hidden, int64_t inter);
+
+/*
+ * Byte offsets of the prefill workspace's parts, for inspection by tests:
+ * offsets[0] counts int32[E], [1] order int32[T*k] (entry index of each
+ * sorted row), [2] {token, weight bits} int32x2[T*k], [3]/[4] tile lists,
+ * [5] tile counts, [6] Xs FP16 [T*k][hidden] (gathered rows), [7] Hs FP16
+ * [T*k][inter] (SwiGLU output), [8] total.  Xs and Hs store each 32-input
+ * block interleaved: position 2j holds input j and 2j+1 input j+16.
+ */
+moex_status moex_moe_prefill_workspace_layout(int T, int k, int E, int64_t hidden, int64_t inter,
+                                              size_t* offsets);
+
+/*
+ * The grouped MoE prefill layer on FP16 tensor cores (#2356 Summary: prompt
+ * rows sorted by expert, IQ4_NL weights dequantised to FP16 per tile with
+ * FP32 sums; #1525 Change: one rounding per dequantised value, SwiGLU
+ * between the products, the top-k combine):
+ *   rows sorted by expert (stable), Xs = fp16(x), Wh = fp16_rn(d * kvalue)
+ *   H  = fp16(silu(g) * u),  g, u = Wh_gu[e] . Xs   (FP32 accumulation)
+ *   out[t] = sum_k w[t,k] * (Wh_dn[e] . H)          (FP32, summed with
+ *            atomic adds: the order of the k terms is not fixed)
+ *   gate_up, down : IQ4_NL stacks [E][2*inter][hidden], [E][hidden][inter].
+ *   x_bf16 : device BF16 [T][hidden];  ids, w : device [T][k] (from
+ *            moex_route_topk); out : device FP32 [T][hidden] (overwritten).
+ *   ws     : device workspace of moex_moe_prefill_workspace_bytes() bytes.
+ * hidden % 128 == 0, inter % 64 == 0.  Six launches (count, place, gather,
+ * GEMM 1, clear, GEMM 2); the GEMMs use tcgen05 / TMEM / TMA.
+ */
+moex_status moex_moe_prefill(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16, int T,
+                             const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,
+                             moex_stream stream);
+
 /*
  * Reads and clears the device status word after synchronising `stream`.
  * *flags receives its bits (1: routing id out of range, 2: copy-pipeline

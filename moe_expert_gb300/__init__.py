@@ -59,6 +59,10 @@ SIGNATURES = {
     "moex_moe_decode_debug": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _SZ,
                                              _P, _P, _P, _P, _P]),
     "moex_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
+    "moex_moe_prefill_workspace_bytes": (_SZ, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _I64, _I64]),
+    "moex_moe_prefill_workspace_layout": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _I64, _I64,
+                                                         ctypes.POINTER(_SZ)]),
+    "moex_moe_prefill": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _SZ, _P]),
 }
 
 _lib = None
@@ -253,6 +257,35 @@ def moe_decode(gate_up: PackedWeight, down: PackedWeight, x, ids, w, out=None, w
                                        _ptr(dbg["gu"]), _ptr(dbg["h"]), _ptr(dbg["hq"]), _ptr(dbg["hds"]), st),
            "moex_moe_decode_debug")
     return out, dbg
+
+
+def moe_prefill_workspace_bytes(T: int, k: int, E: int, hidden: int, inter: int) -> int:
+    return int(lib().moex_moe_prefill_workspace_bytes(T, k, E, hidden, inter))
+
+
+def moe_prefill_workspace_layout(T: int, k: int, E: int, hidden: int, inter: int):
+    """Byte offsets of the prefill workspace parts (see include/moex.h)."""
+    off = (ctypes.c_size_t * 9)()
+    _check(lib().moex_moe_prefill_workspace_layout(T, k, E, hidden, inter, off), "moex_moe_prefill_workspace_layout")
+    return [int(v) for v in off]
+
+
+def moe_prefill(gate_up: PackedWeight, down: PackedWeight, x_bf16, ids, w, out=None, ws=None, stream=None):
+    """The grouped MoE prefill layer.  x_bf16: BF16 (or raw uint16/int16 bit
+    patterns) [T, hidden]; ids / w [T, k].  Returns out [T, hidden] FP32."""
+    torch = _torch()
+    T, hidden = x_bf16.shape
+    k = ids.shape[1]
+    E, inter = gate_up.n_mats, down.K
+    if out is None:
+        out = torch.empty((T, hidden), dtype=torch.float32, device=x_bf16.device)
+    if ws is None:
+        ws = torch.empty(moe_prefill_workspace_bytes(T, k, E, hidden, inter), dtype=torch.uint8,
+                         device=x_bf16.device)
+    _check(lib().moex_moe_prefill(ctypes.byref(gate_up.struct), ctypes.byref(down.struct), _ptr(x_bf16), T,
+                                  _ptr(ids), _ptr(w), k, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           "moex_moe_prefill")
+    return out
 
 
 def device_status(stream=None) -> int:

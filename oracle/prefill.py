@@ -57,15 +57,16 @@ def sort_entries(ids: np.ndarray, n_experts: int):
 
 
 class ExpertCache:
-    """Dequantised FP16 experts, built on first use."""
+    """Dequantised FP16 experts, built on first use (kept as float16, handed
+    out as float64; every FP16 value is exact in float64)."""
 
     def __init__(self, fmt: str, blocks_of):
         self.fmt, self.blocks_of, self.cache = fmt, blocks_of, {}
 
     def __getitem__(self, e: int) -> np.ndarray:
         if e not in self.cache:
-            self.cache[e] = dequant_fp16(self.fmt, self.blocks_of[e]).astype(np.float64)
-        return self.cache[e]
+            self.cache[e] = dequant_fp16(self.fmt, self.blocks_of[e])
+        return self.cache[e].astype(np.float64)
 
 
 def moe_prefill(gate_up, down, x_bf16: np.ndarray, ids: np.ndarray, w: np.ndarray,
