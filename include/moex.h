@@ -217,6 +217,29 @@ moex_status moex_moe_prefill(const moex_qweight* gate_up, const moex_qweight* do
                              moex_stream stream);
 
 /*
+ * moex_moe_decode without a workspace argument, for callers that cannot
+ * allocate device memory (code running inside another framework's memory
+ * pool with no allocator hook, plug-ins that may not allocate after
+ * start-up, decode paths that must never call cudaMalloc).  There is no
+ * counterpart on the pages this library follows; it is a convenience of the
+ * library.
+ *   The workspace is a 512 KiB buffer compiled into the library (a
+ *   __device__ array that every GPU loading the library keeps until the
+ *   process exits).  Layers whose moex_moe_decode_workspace_bytes() exceeds
+ *   512 KiB are rejected with MOEX_ENOSPACE.  Nothing is allocated.
+ *   The first call on a device looks up the buffer's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   Every call on a device uses the same buffer, which keeps the previous
+ *   call's contents (nothing in it needs clearing: the layer writes every
+ *   byte it reads).  Calls that may overlap on the GPU -- on different
+ *   streams, or from several threads -- race on the buffer and must be
+ *   serialised by the caller.
+ * Arguments and results are those of moex_moe_decode.
+ */
+moex_status moex_moe_decode_noalloc(const moex_qweight* gate_up, const moex_qweight* down, const float* x, int T,
+                                    const int32_t* ids, const float* w, int k, float* out, moex_stream stream);
+
+/*
  * Reads and clears the device status word after synchronising `stream`.
  * *flags receives its bits (1: routing id out of range, 2: copy-pipeline
  * wait ran out, 4: tensor-core wait ran out, 8: bad shape on the device).

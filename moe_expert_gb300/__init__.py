@@ -63,6 +63,7 @@ SIGNATURES = {
     "moex_moe_prefill_workspace_layout": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _I64, _I64,
                                                          ctypes.POINTER(_SZ)]),
     "moex_moe_prefill": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _SZ, _P]),
+    "moex_moe_decode_noalloc": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P]),
 }
 
 _lib = None
@@ -285,6 +286,20 @@ def moe_prefill(gate_up: PackedWeight, down: PackedWeight, x_bf16, ids, w, out=N
     _check(lib().moex_moe_prefill(ctypes.byref(gate_up.struct), ctypes.byref(down.struct), _ptr(x_bf16), T,
                                   _ptr(ids), _ptr(w), k, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
            "moex_moe_prefill")
+    return out
+
+
+def moe_decode_noalloc(gate_up: PackedWeight, down: PackedWeight, x, ids, w, out=None, stream=None):
+    """moe_decode on the library's built-in workspace, for callers that
+    cannot allocate device memory (see include/moex.h)."""
+    torch = _torch()
+    T, hidden = x.shape
+    k = ids.shape[1]
+    if out is None:
+        out = torch.empty((T, hidden), dtype=torch.float32, device=x.device)
+    _check(lib().moex_moe_decode_noalloc(ctypes.byref(gate_up.struct), ctypes.byref(down.struct), _ptr(x), T,
+                                         _ptr(ids), _ptr(w), k, _ptr(out), _stream(stream)),
+           "moex_moe_decode_noalloc")
     return out
 
 
