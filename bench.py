@@ -47,6 +47,15 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def peak_fp16():
+    """Dense FP16 tensor peak in TFLOP/s: the measured BF16 cuBLAS burst figure
+    (FP16 and BF16 run at the same tcgen05 rate)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return json.load(open(p)).get("bf16_tflops", 1900.0)
+    return 1900.0
+
+
 # ---------------------------------------------------------------- distributed
 
 def dist_setup(n_gpus):
@@ -272,6 +281,45 @@ def decode_layer_detail(reps, copies=3):
             "weight_bytes": wbytes, "weight_GBps": round(wbytes / (t2 / reps) / 1e9, 1)}
 
 
+def prefill_layer_detail(reps=5, peak_tflops=None):
+    """Grouped MoE prefill layer: 8192 tokens x top-8 of 128 IQ4_NL experts,
+    hidden 2560, inter 1536 (route + sort + gather + two tcgen05 GEMMs)."""
+    import torch
+    import moe_expert_gb300 as mx
+    T, E, k, hidden, inter = 8192, 128, 8, 2560, 1536
+    gu = mx.PackedWeight("iq4_nl", E, 2 * inter, hidden)
+    dn = mx.PackedWeight("iq4_nl", E, hidden, inter)
+    for e in range(E):
+        gu.pack_matrix(e, synth.expert_blocks("gate_up", e, hidden, inter, "iq4_nl"))
+        dn.pack_matrix(e, synth.expert_blocks("down", e, hidden, inter, "iq4_nl"))
+    x = torch.from_numpy(synth.prefill_tokens(T, hidden).view(np.int16)).cuda()
+    logits = torch.from_numpy(synth.prefill_logits(T, E)).cuda()
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    out = torch.empty((T, hidden), dtype=torch.float32, device="cuda")
+    ws = torch.empty(mx.moe_prefill_workspace_bytes(T, k, E, hidden, inter), dtype=torch.uint8, device="cuda")
+
+    def layer():
+        mx.route_topk(logits, k, ids, w)
+        mx.moe_prefill(gu, dn, x, ids, w, out, ws)
+    for _ in range(2):
+        layer()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        layer()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / reps
+    flops = 2.0 * T * k * (2 * inter * hidden + hidden * inter)
+    d = {"tokens": T, "experts": E, "top_k": k, "layer_ms": round(t * 1e3, 3),
+         "algorithmic_tflop": round(flops / 1e12, 4), "layer_tflops": round(flops / t / 1e12, 1)}
+    if peak_tflops:
+        d["frac_of_fp16_dense_peak"] = round(flops / t / 1e12 / peak_tflops, 3)
+    return d
+
+
 def run_ours(args, ws, rank, local):
     import torch
     import moe_expert_gb300 as mx
@@ -357,6 +405,8 @@ def run_ours(args, ws, rank, local):
         del small
         torch.cuda.empty_cache()
         detail["moe_decode_20_experts"] = decode_layer_detail(500)
+        torch.cuda.empty_cache()
+        detail["moe_prefill_8192_tokens"] = prefill_layer_detail(5, peak_fp16())
 
     cpu = cpu_baseline(budget_s=args.cpu_budget) if (rank == 0 and not args.no_cpu) else None
     if rank != 0:
@@ -480,6 +530,14 @@ def run_only(args):
         case = GemvCase(fmt, rows, K, (c,), l2)
         mx.quantize_q8_1(case.x[c], case.xq[c], case.xds[c])
         fn = lambda i: mx.qgemv(case.W[i % case.ncopies], case.xq[c], case.xds[c], case.y[c])  # noqa: E731
+    elif args.only == "prefill":
+        d = prefill_layer_detail(max(1, args.steps), peak_fp16())
+        print(json.dumps({"only": "prefill", **d}))
+        return
+    elif args.only == "decode":
+        d = decode_layer_detail(max(1, args.steps))
+        print(json.dumps({"only": "decode", **d}))
+        return
     else:
         raise SystemExit(f"unknown --only {args.only}")
     for i in range(args.warmup):
@@ -495,7 +553,7 @@ def run_only(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--only", default=None, help="profile helper: gemv_q8_0 | gemv_iq4_nl")
+    ap.add_argument("--only", default=None, help="profile helper: gemv_q8_0 | gemv_iq4_nl | decode | prefill")
     ap.add_argument("--ncols", type=int, default=1)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)

@@ -21,7 +21,11 @@
 // rounded to 16, K = 16) into a double-buffered FP32 accumulator in TMEM, and
 // four epilogue warps read it back with tcgen05.ld.  Because the token count
 // of an expert is the MMA's N, ragged experts cost at most 15 padded columns
-// per tile instead of a partial 128-row M tile.
+// per tile instead of a partial 128-row M tile.  CTAs run in clusters of two
+// on the same token tile (neighbouring feature tiles): each loads half of the
+// token boxes with TMA multicast into both, since one SM's TMA unit cannot
+// feed an M = 128 MMA from L2 at full rate, and each CTA's MMA completion is
+// committed to the release barriers of both.
 //
 // K order: every FP16 operand of the two GEMMs stores each 32-input block
 // interleaved (position 2j = input j, 2j+1 = input j+16), the order in which
@@ -41,10 +45,13 @@ namespace moex {
 constexpr int PF_NMAX = 192;     // tokens per tile (MMA N), multiple of 16
 constexpr int PF_BK = 64;        // inputs per k-step (one 128-byte swizzle row of FP16)
 constexpr int PF_NB_ST = 4;      // B (token) stages in shared memory
+constexpr int PF_BOXR = 32;      // token rows per TMA box
 constexpr int PF_NA_ST = 4;      // A (weight) stages in TMEM
 constexpr int PF_STAGE_B = PF_NMAX * PF_BK * 2;   // bytes of one B stage
 constexpr int PF_ACOL = 2 * PF_NMAX;              // first TMEM column of the A stages
-constexpr int PF_THREADS = 320;  // warp 0 TMA, 1 MMA + TMEM, 2-5 dequant, 6-9 epilogue
+constexpr int PF_DQ_WARPS = 8;   // dequantising warps: two per TMEM lane quarter, one IQ4_NL block each
+constexpr int PF_THREADS = (2 + PF_DQ_WARPS + 4) * 32;  // warp 0 TMA, 1 MMA + TMEM, dequant, 4 epilogue
+constexpr int PF_EPI0 = 2 + PF_DQ_WARPS;                // first epilogue warp
 
 // ----------------------------------------------------------------- sort
 
@@ -203,31 +210,48 @@ struct GemmArgs {
   uint32_t* status;
 };
 
-// Dequantises 64 inputs (2 IQ4_NL blocks) of one weight row into 32 TMEM
-// column words: word 16*b + j = half2(d_b * kv[lo(byte j)], d_b * kv[hi(byte j)]),
-// each product rounded once to FP16 (exact small integer times the FP16
-// scale, one HMUL2 rounding).
-__device__ __forceinline__ void dequant_k64(uint4 n0, uint4 n1, uint32_t sw, uint32_t (&col)[32]) {
+// The IQ4_NL codebook plus 128, as unsigned bytes: entries 0..7 (bit 7
+// clear) and entries 8..15 with bit 7 cleared.
+constexpr uint32_t IQ4B_LO_0 = 0x3F2D1801u;   // 1, 24, 45, 63
+constexpr uint32_t IQ4B_LO_1 = 0x766A5D4Fu;   // 79, 93, 106, 118
+constexpr uint32_t IQ4B_HI_0 = 0x26190D01u;   // 129, 141, 153, 166 & 0x7f
+constexpr uint32_t IQ4B_HI_1 = 0x71594535u;   // 181, 197, 217, 241 & 0x7f
+
+// kvalues[n] + 128 for the four indices in the low 16 bits of `sel`
+// (selector nibble bit 3 flipped in `sel_flipped`): the low entries come
+// from one prmt (zero where n >= 8), the high ones with bit 7 cleared from a
+// second (zero where n < 8), and bit 7 is set where the high part is non-zero
+// (every high entry has a non-zero low part).
+__device__ __forceinline__ uint32_t iq4nl_biased4(uint32_t sel, uint32_t sel_flipped) {
+  const uint32_t lo = prmt(IQ4B_LO_0, IQ4B_LO_1, sel);
+  const uint32_t hi7 = prmt(IQ4B_HI_0, IQ4B_HI_1, sel_flipped);
+  const uint32_t b7 = (hi7 + 0x7F7F7F7Fu) & 0x80808080u;
+  return lo | hi7 | b7;
+}
+
+// Dequantises one IQ4_NL block (16 index bytes n, FP16 scale d) of one weight
+// row into 16 TMEM column words: word j = half2(d * kv[lo(byte j)],
+// d * kv[hi(byte j)]), each product rounded once to FP16 (an exact small
+// integer times the FP16 scale, one HMUL2 rounding).  The integer is made
+// exactly as FP16 from the biased byte u = kv + 128: the half with bits
+// 0x6400 | u is 1024 + u, minus 1152.
+__device__ __forceinline__ void dequant_block16(uint4 n, uint16_t dbits, uint32_t (&col)[16]) {
   const __half2 one152 = __half2half2(__ushort_as_half(0x6480));  // 1152
-  const uint32_t W[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+  const __half2 d2 = __half2half2(__ushort_as_half(dbits));
+  const uint32_t W[4] = {n.x, n.y, n.z, n.w};
 #pragma unroll
-  for (int bb = 0; bb < 2; ++bb) {
-    const __half2 d2 = __half2half2(__ushort_as_half(static_cast<uint16_t>(bb ? (sw >> 16) : (sw & 0xFFFFu))));
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t wv = W[i];
+    const uint32_t fl = wv ^ 0x88888888u;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t wv = W[4 * bb + i];
-      const uint32_t fl = wv ^ 0x88888888u;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const uint32_t v = iq4nl_lookup4(hh ? (wv >> 16) : wv, hh ? (fl >> 16) : fl);  // 4 int8
-        const uint32_t u = v ^ 0x80808080u;  // v + 128 as unsigned bytes
-        const uint32_t p0 = prmt(u, 0x64646464u, 0x4140u);  // half2(1024 + u0, 1024 + u1)
-        const uint32_t p1 = prmt(u, 0x64646464u, 0x4342u);
-        __half2 h0 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p0), one152), d2);
-        __half2 h1 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p1), one152), d2);
-        col[16 * bb + 4 * i + 2 * hh] = *reinterpret_cast<uint32_t*>(&h0);
-        col[16 * bb + 4 * i + 2 * hh + 1] = *reinterpret_cast<uint32_t*>(&h1);
-      }
+    for (int hh = 0; hh < 2; ++hh) {
+      const uint32_t u = iq4nl_biased4(hh ? (wv >> 16) : wv, hh ? (fl >> 16) : fl);
+      const uint32_t p0 = prmt(u, 0x64646464u, 0x4140u);  // half2(1024 + u0, 1024 + u1)
+      const uint32_t p1 = prmt(u, 0x64646464u, 0x4342u);
+      __half2 h0 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p0), one152), d2);
+      __half2 h1 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p1), one152), d2);
+      col[4 * i + 2 * hh] = *reinterpret_cast<uint32_t*>(&h0);
+      col[4 * i + 2 * hh + 1] = *reinterpret_cast<uint32_t*>(&h1);
     }
   }
 }
@@ -279,7 +303,8 @@ struct PfSmem {
 };
 
 // EPI == 1: SwiGLU -> H (FP16).  EPI == 2: weighted combine into out.
-template <int EPI>
+// CL == 2: clusters of two CTAs sharing each token stage (multicast); CL == 1: alone.
+template <int EPI, int CL>
 __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __grid_constant__ CUtensorMap bmap,
                                                                      GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -302,10 +327,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   if (threadIdx.x == 0) {
     for (int i = 0; i < PF_NB_ST; ++i) {
       mbar_init(&b_full[i], 1);
-      mbar_init(&b_empty[i], 1);
+      mbar_init(&b_empty[i], CL);  // the MMAs of every CTA of the cluster
     }
     for (int i = 0; i < PF_NA_ST; ++i) {
-      mbar_init(&a_full[i], 128);
+      mbar_init(&a_full[i], PF_DQ_WARPS * 32);
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -323,11 +348,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   }
   tc_fence_before();
   __syncthreads();
+  if (CL == 2) cluster_sync_all();  // both CTAs' barriers are initialised before any multicast lands
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
   pdl_wait();  // tiles, tokens and (GEMM 2) H come from earlier kernels
   pdl_launch_dependents();
+  // tiles 2p and 2p+1 (same expert and tokens, neighbouring feature tiles)
+  // go to the two CTAs of one cluster
+  const int rank = CL == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int t0 = CL == 2 ? 2 * (blockIdx.x >> 1) + rank : blockIdx.x;
+  const int tstep = CL == 2 ? 2 * (gridDim.x >> 1) : gridDim.x;
   const int ntiles = *a.ntiles;
   const int KS = a.K / PF_BK;
 
@@ -335,9 +366,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
     // ------------------------------------------------ B producer (TMA)
     if (lane == 0) {
       int kc = 0;
-      for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x) {
+      for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
         const int4 tile = a.tiles[t];
-        const int nbox = (tile.w + 31) / 32;
+        const int nbox = (tile.w + PF_BOXR - 1) / PF_BOXR;
         for (int ks = 0; ks < KS; ++ks, ++kc) {
           const int s = kc % PF_NB_ST;
           if (kc >= PF_NB_ST && !mbar_wait(&b_empty[s], ((kc / PF_NB_ST) - 1) & 1, abort_flag)) {
@@ -345,10 +376,21 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
             flag_status(a.status, DEV_TIMEOUT_MMA);
             break;
           }
-          mbar_arrive_expect_tx(&b_full[s], nbox * 32 * PF_BK * 2);
-          for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(sb + s * PF_STAGE_B + bx * 32 * PF_BK * 2, &bmap, ks * PF_BK, tile.z + 32 * bx, &b_full[s]);
+          // the whole stage lands in this CTA (with CL == 2, half of the boxes from each CTA of the pair)
+          mbar_arrive_expect_tx(&b_full[s], nbox * PF_BOXR * PF_BK * 2);
+          for (int bx = rank; bx < nbox; bx += CL) {
+            uint8_t* dst = sb + s * PF_STAGE_B + bx * PF_BOXR * PF_BK * 2;
+            if (CL == 2)
+              tma_load_2d_mc(dst, &bmap, ks * PF_BK, tile.z + PF_BOXR * bx, &b_full[s], 0x3);
+            else
+              tma_load_2d(dst, &bmap, ks * PF_BK, tile.z + PF_BOXR * bx, &b_full[s]);
+          }
         }
+      }
+      // after an abort, let the copies already issued land before the CTA exits
+      if (*abort_flag) {
+        for (int j = kc - 1; j >= 0 && j >= kc - PF_NB_ST; --j)
+          mbar_wait(&b_full[j % PF_NB_ST], (j / PF_NB_ST) & 1, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -356,7 +398,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
     if (lane == 0) {
       int kc = 0, ti = 0;
       bool issued_any = false;
-      for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x, ++ti) {
+      for (int t = t0; t < ntiles && !*abort_flag; t += tstep, ++ti) {
         const int4 tile = a.tiles[t];
         const int ab = ti & 1;
         if (ti >= 2 && !mbar_wait(&d_empty[ab], ((ti >> 1) - 1) & 1, abort_flag)) {
@@ -384,7 +426,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
           }
           issued_any = true;
           mma_commit(&a_empty[sa]);
-          mma_commit(&b_empty[sbk]);
+          if (CL == 2)
+            mma_commit_mc(&b_empty[sbk], 0x3);  // both CTAs' B stage is refilled once both MMAs are done
+          else
+            mma_commit(&b_empty[sbk]);
         }
         if (*abort_flag) break;
         mma_commit(&d_full[ab]);
@@ -395,12 +440,16 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
         mbar_wait(done_bar, 0, nullptr);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < PF_EPI0) {
     // ------------------------------------------------ A producers: dequantise into TMEM
+    // warp pair (w, w + 4) shares lane quarter q; half h dequantises block h
+    // of each 64-input k-step (TMEM columns 16h .. 16h+15 of the stage).
     const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
     const int m = 32 * q + lane;  // A row = TMEM lane
+    constexpr int PD = 3;         // k-steps of raw bytes in flight per thread
     int kc = 0;
-    for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x) {
+    for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
       const int4 tile = a.tiles[t];
       int64_t row;
       if (EPI == 1) {
@@ -409,21 +458,31 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
       } else {
         row = static_cast<int64_t>(tile.x) * a.rows_per_expert + tile.y * 128 + m;
       }
-      const uint8_t* qp = a.qs + row * a.qrow;
-      const uint8_t* sp = a.sc + row * a.scrow;
-      uint4 n0 = ldg_nc_v4(qp), n1 = ldg_nc_v4(qp + 16);
-      uint32_t sw = ldg_nc_u32(sp);
-      for (int ks = 0; ks < KS; ++ks, ++kc) {
-        // next k-step's raw bytes in flight while this one is decoded
-        uint4 m0 = n0, m1 = n1;
-        uint32_t msw = sw;
-        if (ks + 1 < KS) {
-          n0 = ldg_nc_v4(qp + (ks + 1) * 32);
-          n1 = ldg_nc_v4(qp + (ks + 1) * 32 + 16);
-          sw = ldg_nc_u32(sp + (ks + 1) * 4);
+      const uint8_t* qp = a.qs + row * a.qrow + 16 * h;
+      const uint16_t* sp = reinterpret_cast<const uint16_t*>(a.sc + row * a.scrow) + h;
+      uint4 rq[PD];
+      uint16_t rs[PD];
+#pragma unroll
+      for (int i = 0; i < PD; ++i) {
+        if (i < KS) {
+          rq[i] = ldg_nc_v4(qp + i * 32);
+          rs[i] = __ldg(sp + 2 * i);
         }
-        uint32_t col[32];
-        dequant_k64(m0, m1, msw, col);
+      }
+      for (int ks = 0; ks < KS; ++ks, ++kc) {
+        const uint4 cq = rq[0];
+        const uint16_t cs = rs[0];
+#pragma unroll
+        for (int i = 0; i + 1 < PD; ++i) {
+          rq[i] = rq[i + 1];
+          rs[i] = rs[i + 1];
+        }
+        if (ks + PD < KS) {
+          rq[PD - 1] = ldg_nc_v4(qp + (ks + PD) * 32);
+          rs[PD - 1] = __ldg(sp + 2 * (ks + PD));
+        }
+        uint32_t col[16];
+        dequant_block16(cq, cs, col);
         const int s = kc % PF_NA_ST;
         if (kc >= PF_NA_ST && !mbar_wait(&a_empty[s], ((kc / PF_NA_ST) - 1) & 1, abort_flag)) {
           *abort_flag = 1;
@@ -431,7 +490,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
           break;
         }
         tc_fence_after();
-        tmem_st32(tmem + (static_cast<uint32_t>(32 * q) << 16) + PF_ACOL + s * 32, col);
+        tmem_st16(tmem + (static_cast<uint32_t>(32 * q) << 16) + PF_ACOL + s * 32 + 16 * h, col);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&a_full[s]);
@@ -441,7 +500,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
     // ------------------------------------------------ epilogue
     const int q = warp & 3;
     int ti = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++ti) {
+    for (int t = t0; t < ntiles; t += tstep, ++ti) {
       const int4 tile = a.tiles[t];
       const int ab = ti & 1;
       bool stop = *abort_flag != 0;
@@ -477,7 +536,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
               if (p < tile.w) {
                 const float g = __uint_as_float(r[i]);
                 const float u = xb[lane * 33 + i];
-                const float h = __fmul_rn(__fdiv_rn(g, 1.0f + expf(-g)), u);
+                const float h = __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
                 a.Hs[static_cast<int64_t>(tile.z + p) * a.I + col] = __float2half_rn(h);
               }
             }
@@ -500,6 +559,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   }
   tc_fence_before();
   __syncthreads();
+  if (CL == 2) cluster_sync_all();  // no multicast copy or commit of the partner is still in flight
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -526,13 +586,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D FP16 map over [rows][cols] (row pitch cols*2 bytes), box 64 x 32, 128-byte swizzle.
+// 2-D FP16 map over [rows][cols] (row pitch cols*2 bytes), box 64 x PF_BOXR, 128-byte swizzle.
 bool make_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
-  const cuuint32_t box[2] = {PF_BK, 32};
+  const cuuint32_t box[2] = {PF_BK, PF_BOXR};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -540,6 +600,54 @@ bool make_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
 }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+using PfKernel = void (*)(CUtensorMap, GemmArgs);
+
+cudaLaunchConfig_t pf_config(int grid, size_t smem, cudaStream_t s, int cl, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(PF_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cl;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cfg;
+}
+
+// Persistent grid: every CTA (cluster) resident at once.  For pairs this is
+// twice the number of co-resident clusters, which can be below the SM count
+// when a GPC has an odd number of free SMs.
+int pf_grid(PfKernel kern, int cl, size_t smem) {
+  if (cl == 1) return sm_count();
+  static int cached[2] = {0, 0};
+  static PfKernel which[2] = {nullptr, nullptr};
+  for (int i = 0; i < 2; ++i)
+    if (which[i] == kern) return cached[i];
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pf_config(sm_count(), smem, nullptr, cl, attr);
+  int nclusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess || nclusters <= 0) {
+    cudaGetLastError();
+    nclusters = sm_count() / 2;
+  }
+  const int slot = which[0] == nullptr ? 0 : 1;
+  which[slot] = kern;
+  cached[slot] = 2 * nclusters;
+  return cached[slot];
+}
+
+cudaError_t launch_pf_gemm(PfKernel kern, int cl, size_t smem, cudaStream_t s, const CUtensorMap& map,
+                           const GemmArgs& args) {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pf_config(pf_grid(kern, cl, smem), smem, s, cl, attr);
+  return cudaLaunchKernelEx(&cfg, kern, map, args);
+}
 
 }  // namespace
 
@@ -590,18 +698,21 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   CUtensorMap m1, m2;
   if (!make_map(&m1, xs, n, H) || !make_map(&m2, hs, n, I)) return MOEX_ECUDA;
 
-  cudaError_t e;
-  if ((e = launch_pdl(prefill_count_kernel, dim3(E), dim3(256), 0, s, ids, n, E, counts, status)) != cudaSuccess)
+  if (launch_pdl(prefill_count_kernel, dim3(E), dim3(256), 0, s, ids, n, E, counts, status) != cudaSuccess)
     return MOEX_ECUDA;
-  if ((e = launch_pdl(prefill_place_kernel, dim3(E), dim3(256), 0, s, ids, w, n, k, E,
-                      static_cast<const int*>(counts), order, tokw, tl)) != cudaSuccess)
+  if (launch_pdl(prefill_place_kernel, dim3(E), dim3(256), 0, s, ids, w, n, k, E, static_cast<const int*>(counts),
+                 order, tokw, tl) != cudaSuccess)
     return MOEX_ECUDA;
-  if ((e = launch_pdl(prefill_gather_kernel, dim3((n * 32 + 255) / 256), dim3(256), 0, s, x, H, k, n,
-                      static_cast<const int*>(order), xs)) != cudaSuccess)
+  if (launch_pdl(prefill_gather_kernel, dim3((n * 32 + 255) / 256), dim3(256), 0, s, x, H, k, n,
+                 static_cast<const int*>(order), xs) != cudaSuccess)
     return MOEX_ECUDA;
   const PfSmem L;
-  if (ensure_smem(reinterpret_cast<const void*>(prefill_gemm_kernel<1>), L.total) != cudaSuccess ||
-      ensure_smem(reinterpret_cast<const void*>(prefill_gemm_kernel<2>), L.total) != cudaSuccess)
+  // pairs share each token stage when both GEMMs have an even number of feature tiles
+  const int cl = (tl.F1 % 2 == 0 && tl.F2 % 2 == 0) ? 2 : 1;
+  const PfKernel k1 = cl == 2 ? prefill_gemm_kernel<1, 2> : prefill_gemm_kernel<1, 1>;
+  const PfKernel k2 = cl == 2 ? prefill_gemm_kernel<2, 2> : prefill_gemm_kernel<2, 1>;
+  if (ensure_smem(reinterpret_cast<const void*>(k1), L.total) != cudaSuccess ||
+      ensure_smem(reinterpret_cast<const void*>(k2), L.total) != cudaSuccess)
     return MOEX_ECUDA;
   GemmArgs g1 = {};
   g1.qs = static_cast<const uint8_t*>(gu->qs);
@@ -615,9 +726,7 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   g1.Hs = hs;
   g1.I = I;
   g1.status = status;
-  const int grid = sm_count();
-  if (launch_pdl(prefill_gemm_kernel<1>, dim3(grid), dim3(PF_THREADS), L.total, s, m1, g1) != cudaSuccess)
-    return MOEX_ECUDA;
+  if (launch_pf_gemm(k1, cl, L.total, s, m1, g1) != cudaSuccess) return MOEX_ECUDA;
   if (cudaMemsetAsync(out, 0, static_cast<size_t>(T) * H * sizeof(float), s) != cudaSuccess) return MOEX_ECUDA;
   GemmArgs g2 = {};
   g2.qs = static_cast<const uint8_t*>(dn->qs);
@@ -632,8 +741,7 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   g2.Hd = H;
   g2.tokw = tokw;
   g2.status = status;
-  if (launch_pdl(prefill_gemm_kernel<2>, dim3(grid), dim3(PF_THREADS), L.total, s, m2, g2) != cudaSuccess)
-    return MOEX_ECUDA;
+  if (launch_pf_gemm(k2, cl, L.total, s, m2, g2) != cudaSuccess) return MOEX_ECUDA;
   return MOEX_OK;
 }
 
