@@ -187,9 +187,11 @@ size_t moex_moe_prefill_workspace_bytes(int T, int k, int E, int64_t hidden, int
 
 /*
  * Byte offsets of the prefill workspace's parts, for inspection by tests:
- * offsets[0] counts int32[E], [1] order int32[T*k] (entry index of each
- * sorted row), [2] {token, weight bits} int32x2[T*k], [3]/[4] tile lists,
- * [5] tile counts, [6] Xs FP16 [T*k][hidden] (gathered rows), [7] Hs FP16
+ * offsets[0] counts int32[E] (then the sort's per-segment histograms and
+ * per-expert offsets), [1] order int32[T*k] (entry index of each sorted row),
+ * [2] {token, weight bits} int32x2[T*k], [3]/[4] tile lists, [5] totals
+ * int32[4] (GEMM 1 tiles, GEMM 2 tiles, placed rows, token tiles), [6] Xs
+ * FP16 [T*k][hidden] (gathered rows), [7] Hs FP16
  * [T*k][inter] (SwiGLU output), [8] total.  Xs and Hs store each 32-input
  * block interleaved: position 2j holds input j and 2j+1 input j+16.
  */
@@ -209,8 +211,10 @@ moex_status moex_moe_prefill_workspace_layout(int T, int k, int E, int64_t hidde
  *   x_bf16 : device BF16 [T][hidden];  ids, w : device [T][k] (from
  *            moex_route_topk); out : device FP32 [T][hidden] (overwritten).
  *   ws     : device workspace of moex_moe_prefill_workspace_bytes() bytes.
- * hidden % 128 == 0, inter % 64 == 0.  Six launches (count, place, gather,
- * GEMM 1, clear, GEMM 2); the GEMMs use tcgen05 / TMEM / TMA.
+ * hidden % 128 == 0, inter % 64 == 0, E <= 4096, E * 2 * inter < 2^31.
+ * Eight launches (sort: histogram, scan, tiles, scatter; gather; GEMM 1;
+ * clear; GEMM 2); the GEMMs use tcgen05 / TMEM / TMA.  An entry whose id is
+ * outside [0, E) is left out of the layer and flagged (MOEX_EDEVICE).
  */
 moex_status moex_moe_prefill(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16, int T,
                              const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,

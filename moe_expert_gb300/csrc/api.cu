@@ -231,6 +231,8 @@ moex_status moex_moe_prefill(const moex_qweight* gate_up, const moex_qweight* do
   if (gate_up->n_mats != down->n_mats || gate_up->n_mats > 4096) return MOEX_EINVAL;
   if (gate_up->rows % 2 != 0 || down->rows != gate_up->K || down->K != gate_up->rows / 2) return MOEX_EINVAL;
   if (gate_up->K % 128 != 0 || down->K % 64 != 0) return MOEX_EUNSUPPORTED;
+  // weight rows are 32-bit tensor-map coordinates
+  if (static_cast<int64_t>(gate_up->n_mats) * gate_up->rows > INT32_MAX) return MOEX_EUNSUPPORTED;
   if (ws_bytes < moe_prefill_ws_bytes(T, k, gate_up->n_mats, gate_up->K, down->K)) return MOEX_ENOSPACE;
   if (!aligned16(x_bf16) || !aligned16(ws) || !aligned16(out)) return MOEX_EALIGN;
   return launch_moe_prefill(gate_up, down, x_bf16, T, ids, w, k, out, ws, stream);

@@ -45,151 +45,243 @@ namespace moex {
 constexpr int PF_NMAX = 192;     // tokens per tile (MMA N), multiple of 16
 constexpr int PF_BK = 64;        // inputs per k-step (one 128-byte swizzle row of FP16)
 constexpr int PF_NB_ST = 4;      // B (token) stages in shared memory
-constexpr int PF_BOXR = 32;      // token rows per TMA box
+constexpr int PF_BOXR = 64;      // token rows per TMA box
 constexpr int PF_NA_ST = 4;      // A (weight) stages in TMEM
 constexpr int PF_STAGE_B = PF_NMAX * PF_BK * 2;   // bytes of one B stage
+static_assert(PF_NB_ST == PF_NA_ST, "A and B stages advance together");
 constexpr int PF_ACOL = 2 * PF_NMAX;              // first TMEM column of the A stages
 constexpr int PF_DQ_WARPS = 8;   // dequantising warps: two per TMEM lane quarter, one IQ4_NL block each
-constexpr int PF_THREADS = (2 + PF_DQ_WARPS + 4) * 32;  // warp 0 TMA, 1 MMA + TMEM, dequant, 4 epilogue
-constexpr int PF_EPI0 = 2 + PF_DQ_WARPS;                // first epilogue warp
+constexpr int PF_DQ0 = 3;        // first dequantising warp
+constexpr int PF_THREADS = (3 + PF_DQ_WARPS + 4) * 32;  // warp 0 B TMA, 1 MMA + TMEM, 2 A TMA, dequant, 4 epilogue
+constexpr int PF_EPI0 = PF_DQ0 + PF_DQ_WARPS;           // first epilogue warp
+// Raw weight stages: the IQ4_NL bytes of 128 rows x 4 k-steps (8 blocks a
+// row), two boxes of 64 rows x 128 bytes with the 128-byte swizzle, then
+// their FP16 scales, two boxes of 64 rows x 16 bytes.
+constexpr int PF_RAW_KS = 4;                      // k-steps per raw stage
+constexpr int PF_NR_ST = 4;                       // raw stages
+constexpr int PF_RAW_QS = 128 * 128;              // nibble bytes of a raw stage
+constexpr int PF_RAW_STAGE = PF_RAW_QS + 128 * 16;  // + scale bytes (multiple of 1024)
 
 // ----------------------------------------------------------------- sort
 
-// counts[e] = number of entries routed to expert e (one CTA per expert).
-__global__ void __launch_bounds__(256) prefill_count_kernel(const int32_t* __restrict__ ids, int n, int E,
-                                                            int* __restrict__ counts, uint32_t* status) {
-  pdl_wait();
-  pdl_launch_dependents();
-  const int e = blockIdx.x;
-  int c = 0;
-  for (int j = threadIdx.x; j < n; j += blockDim.x) {
-    const int v = ids[j];
-    c += v == e;
-    if (e == 0 && (v < 0 || v >= E)) flag_status(status, DEV_BAD_ROUTE);
-  }
-  __shared__ int red[8];
-  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int s = 0;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += red[i];
-    counts[e] = s;
-  }
-}
+// Stable counting sort of the T*k entries by expert in three launches:
+// per-segment histograms, one CTA that scans them (expert offsets, segment
+// bases, tile lists), and a per-segment scatter that ranks equal experts
+// in entry order with warp match.  Entries whose id is out of range are
+// flagged and left out (the later kernels only see placed rows).
 
 struct PrefillTiles {
   int4* t1;     // GEMM 1 tiles {expert, feature tile, first row, rows}
   int4* t2;     // GEMM 2 tiles
-  int* n1;      // number of GEMM 1 tiles
+  int* n1;      // number of GEMM 1 tiles; n1[1] GEMM 2 tiles, n1[2] placed rows
   int* n2;
   int F1, F2;   // feature tiles per expert (I/64, H/128)
 };
 
 __host__ __device__ inline int pf_token_tiles(int n) { return (n + PF_NMAX - 1) / PF_NMAX; }
 
-// Stable placement (one CTA per expert): order[off_e + r] = the r-th entry
-// (in entry order) routed to e; tokw[...] = {token, weight}; and the tiles
-// of expert e for both GEMMs: ceil(n_e / 192) token tiles of balanced size,
-// times the feature tiles.
-__global__ void __launch_bounds__(256) prefill_place_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w,
-                                                            int n, int k, int E, const int* __restrict__ counts,
-                                                            int* __restrict__ order, int2* __restrict__ tokw,
+constexpr int PF_MAX_SEGS = 1024;   // at most this many histogram segments
+
+// Entries per segment: a multiple of 32, at least 512, at most PF_MAX_SEGS segments.
+__host__ __device__ inline int pf_seg_len(int n) {
+  int seg = (n + PF_MAX_SEGS - 1) / PF_MAX_SEGS;
+  seg = seg < 512 ? 512 : seg;
+  return (seg + 31) & ~31;
+}
+__host__ __device__ inline int pf_nsegs(int n) { return (n + pf_seg_len(n) - 1) / pf_seg_len(n); }
+
+// hist[s][e] = entries of segment s routed to e (one CTA per segment).
+__global__ void __launch_bounds__(256) prefill_hist_kernel(const int32_t* __restrict__ ids, int n, int E,
+                                                           int* __restrict__ hist, uint32_t* status) {
+  extern __shared__ int h_s[];
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) h_s[e] = 0;
+  __syncthreads();
+  const int seg = pf_seg_len(n);
+  const int j0 = blockIdx.x * seg, j1 = min(n, j0 + seg);
+  for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+    const int v = ids[j];
+    if (v < 0 || v >= E)
+      flag_status(status, DEV_BAD_ROUTE);
+    else
+      atomicAdd(&h_s[v], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<int64_t>(blockIdx.x) * E + e] = h_s[e];
+}
+
+// Exclusive scan of v over the block (blockDim.x == 1024); returns the total.
+__device__ __forceinline__ int block_exscan(int& v, int* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) red[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int t = red[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    red[lane] = t;
+  }
+  __syncthreads();
+  const int total = red[31];
+  v = x - v + (warp ? red[warp - 1] : 0);
+  __syncthreads();
+  return total;
+}
+
+// One CTA of 1024 threads, thread i owns experts 4i .. 4i+3 (E <= 4096):
+// counts, first sorted row eoff[e] and first token tile etb[e] of each
+// expert (etb[E] = all token tiles), hist[s][e] -> first sorted row of
+// segment s's entries for e, and the totals n1[0..3] = GEMM 1 tiles,
+// GEMM 2 tiles, placed rows, token tiles.
+__global__ void __launch_bounds__(1024) prefill_scan_kernel(int n, int E, int* __restrict__ hist,
+                                                            int* __restrict__ counts, int* __restrict__ eoff,
+                                                            int* __restrict__ etb, PrefillTiles tl) {
+  __shared__ int red[32];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int S = pf_nsegs(n);
+  int c[4];
+  int csum = 0, tsum = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = 4 * threadIdx.x + i;
+    int v = 0;
+    if (e < E)
+      for (int sg = 0; sg < S; ++sg) v += hist[static_cast<int64_t>(sg) * E + e];
+    c[i] = v;
+    csum += v;
+    tsum += pf_token_tiles(v);
+  }
+  int off = csum, tb = tsum;
+  const int placed = block_exscan(off, red);
+  const int ttot = block_exscan(tb, red);
+  if (threadIdx.x == 0) {
+    tl.n1[0] = ttot * tl.F1;
+    tl.n1[1] = ttot * tl.F2;
+    tl.n1[2] = placed;
+    tl.n1[3] = ttot;
+    etb[E] = ttot;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = 4 * threadIdx.x + i;
+    if (e >= E) break;
+    counts[e] = c[i];
+    eoff[e] = off;
+    etb[e] = tb;
+    int run = off;
+    for (int sg = 0; sg < S; ++sg) {
+      int* hp = hist + static_cast<int64_t>(sg) * E + e;
+      const int h = *hp;
+      *hp = run;
+      run += h;
+    }
+    off += c[i];
+    tb += pf_token_tiles(c[i]);
+  }
+}
+
+// Both tile lists, one thread per tile: token tile g belongs to the last
+// expert e with etb[e] <= g; its ceil(n_e / 192) token tiles split the
+// expert's rows evenly.
+__global__ void __launch_bounds__(256) prefill_tiles_kernel(int E, const int* __restrict__ counts,
+                                                            const int* __restrict__ eoff, const int* __restrict__ etb,
                                                             PrefillTiles tl) {
   pdl_wait();
   pdl_launch_dependents();
-  const int e = blockIdx.x;
-  __shared__ int s_off, s_tbase, s_wsum[8];
-  if (threadIdx.x == 0) {
-    int off = 0, tb = 0, tot = 0;
-    for (int i = 0; i < E; ++i) {
-      if (i < e) {
-        off += counts[i];
-        tb += pf_token_tiles(counts[i]);
-      }
-      tot += pf_token_tiles(counts[i]);
-    }
-    s_off = off;
-    s_tbase = tb;
-    if (e == E - 1) {
-      *tl.n1 = tot * tl.F1;
-      *tl.n2 = tot * tl.F2;
-    }
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t TT = tl.n1[3];
+  const bool first = i < TT * tl.F1;
+  const int64_t j = first ? i : i - TT * tl.F1;
+  const int F = first ? tl.F1 : tl.F2;
+  if (j >= TT * F) return;
+  const int g = static_cast<int>(j / F), f = static_cast<int>(j % F);
+  int lo = 0, hi = E;  // first e with etb[e] > g is in (lo, hi]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (etb[mid] <= g) lo = mid; else hi = mid - 1;
   }
-  __syncthreads();
-  const int ne = counts[e];
-  const int off = s_off;
-  // tiles
-  const int ntt = pf_token_tiles(ne);
-  for (int i = threadIdx.x; i < ntt * tl.F1; i += blockDim.x) {
-    const int tt = i / tl.F1, f = i % tl.F1;
-    const int r0 = off + tt * ne / ntt, r1 = off + (tt + 1) * ne / ntt;
-    tl.t1[(s_tbase + tt) * tl.F1 + f] = make_int4(e, f, r0, r1 - r0);
-  }
-  for (int i = threadIdx.x; i < ntt * tl.F2; i += blockDim.x) {
-    const int tt = i / tl.F2, f = i % tl.F2;
-    const int r0 = off + tt * ne / ntt, r1 = off + (tt + 1) * ne / ntt;
-    tl.t2[(s_tbase + tt) * tl.F2 + f] = make_int4(e, f, r0, r1 - r0);
-  }
-  // stable compaction of the entries of expert e
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int base = 0;
-  for (int j0 = 0; j0 < n; j0 += blockDim.x) {
-    const int j = j0 + threadIdx.x;
-    const bool mine = j < n && ids[j] == e;
-    const unsigned bal = __ballot_sync(0xffffffffu, mine);
-    if (lane == 0) s_wsum[warp] = __popc(bal);
-    __syncthreads();
-    int before = base;
-    for (int i = 0; i < warp; ++i) before += s_wsum[i];
-    if (mine) {
-      const int r = before + __popc(bal & ((1u << lane) - 1u));
-      order[off + r] = j;
-      tokw[off + r] = make_int2(j / k, __float_as_int(w[j]));
+  const int e = lo;
+  const int64_t ne = counts[e];
+  const int64_t ntt = pf_token_tiles(static_cast<int>(ne));
+  const int64_t tt = g - etb[e];
+  const int r0 = eoff[e] + static_cast<int>(tt * ne / ntt), r1 = eoff[e] + static_cast<int>((tt + 1) * ne / ntt);
+  (first ? tl.t1 : tl.t2)[j] = make_int4(e, f, r0, r1 - r0);
+}
+
+// One warp per segment, entries in order, 32 at a time: equal experts are
+// ranked by lane with __match_any_sync; order[row] = entry, tokw[row] =
+// {token, weight bits}.
+__global__ void __launch_bounds__(32) prefill_scatter_kernel(const int32_t* __restrict__ ids,
+                                                             const float* __restrict__ w, int n, int k, int E,
+                                                             const int* __restrict__ hist, int* __restrict__ order,
+                                                             int2* __restrict__ tokw) {
+  extern __shared__ int run[];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) run[e] = hist[static_cast<int64_t>(blockIdx.x) * E + e];
+  __syncwarp();
+  const int seg = pf_seg_len(n);
+  const int j0 = blockIdx.x * seg, j1 = min(n, j0 + seg);
+  for (int jb = j0; jb < j1; jb += 32) {
+    const int j = jb + lane;
+    const int v = j < j1 ? ids[j] : -1;
+    const bool ok = v >= 0 && v < E;
+    const unsigned peers = __match_any_sync(0xffffffffu, ok ? v : -1);
+    if (ok) {
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int row = run[v] + rank;
+      order[row] = j;
+      tokw[row] = make_int2(j / k, __float_as_int(w[j]));
     }
-    int tot = 0;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += s_wsum[i];
-    base += tot;
-    __syncthreads();
+    __syncwarp();
+    // the highest lane of each group advances the expert's next row
+    if (ok && (peers >> lane) == 1u) run[v] += __popc(peers);
+    __syncwarp();
   }
 }
 
 // ----------------------------------------------------------------- gather
 
-// Xs[p] = fp16(x[token(order[p])]) with each 32-input block interleaved.
-// One warp per sorted row; lane handles whole blocks.
-__global__ void __launch_bounds__(256) prefill_gather_kernel(const uint16_t* __restrict__ x, int H, int k, int n,
+// Xs[p] = fp16(x[token(order[p])]) with each 32-input block interleaved,
+// for the placed rows p < *nrows.  One thread per 16 output bytes: the
+// pairs (j, j+16) for j = 4c .. 4c+3 of a block, from two 8-byte loads.
+__global__ void __launch_bounds__(256) prefill_gather_kernel(const uint16_t* __restrict__ x, int H, int k,
+                                                             const int* __restrict__ nrows,
                                                              const int* __restrict__ order, __half* __restrict__ xs) {
   pdl_wait();
   pdl_launch_dependents();
-  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (row >= n) return;
+  const int per_row = H / 8;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = i / per_row;
+  if (row >= *nrows) return;
+  const int c = static_cast<int>(i - row * per_row);
+  const int blk = c >> 2, cc = c & 3;
   const int t = order[row] / k;
-  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H);
-  uint4* dst = reinterpret_cast<uint4*>(xs + static_cast<int64_t>(row) * H);
-  for (int blk = lane; blk < H / QK; blk += 32) {
-    uint32_t in[16];
+  const uint16_t* src = x + static_cast<int64_t>(t) * H + blk * QK + 4 * cc;
+  const uint2 lo = *reinterpret_cast<const uint2*>(src);        // inputs 4cc .. 4cc+3
+  const uint2 hi = *reinterpret_cast<const uint2*>(src + 16);   // inputs 4cc+16 .. 4cc+19
+  const uint32_t a[4] = {lo.x & 0xFFFFu, lo.x >> 16, lo.y & 0xFFFFu, lo.y >> 16};
+  const uint32_t b[4] = {hi.x & 0xFFFFu, hi.x >> 16, hi.y & 0xFFFFu, hi.y >> 16};
+  uint32_t o[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 v = src[blk * 4 + i];
-      in[4 * i] = v.x; in[4 * i + 1] = v.y; in[4 * i + 2] = v.z; in[4 * i + 3] = v.w;
-    }
-    // element e of the block: 16-bit half (e & 1) of word e >> 1
-    auto elem = [&](int e) -> float {
-      const uint32_t wv = in[e >> 1];
-      const uint16_t b = (e & 1) ? static_cast<uint16_t>(wv >> 16) : static_cast<uint16_t>(wv & 0xFFFFu);
-      return __uint_as_float(static_cast<uint32_t>(b) << 16);
-    };
-    uint32_t o[16];
-#pragma unroll
-    for (int jj = 0; jj < 16; ++jj) {
-      const __half2 h = __halves2half2(__float2half_rn(elem(jj)), __float2half_rn(elem(jj + 16)));
-      o[jj] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) dst[blk * 4 + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+  for (int jj = 0; jj < 4; ++jj) {
+    const __half2 h = __halves2half2(__float2half_rn(__uint_as_float(a[jj] << 16)),
+                                     __float2half_rn(__uint_as_float(b[jj] << 16)));
+    o[jj] = *reinterpret_cast<const uint32_t*>(&h);
   }
+  *reinterpret_cast<uint4*>(xs + row * H + blk * QK + 8 * cc) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // ----------------------------------------------------------------- GEMM
@@ -256,19 +348,6 @@ __device__ __forceinline__ void dequant_block16(uint4 n, uint16_t dbits, uint32_
   }
 }
 
-__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-__device__ __forceinline__ uint32_t ldg_nc_u32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
@@ -288,11 +367,12 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool f
 }
 
 struct PfSmem {
-  int b, bars, xbuf, tmem, abort_flag, total;
+  int b, raw, bars, xbuf, tmem, abort_flag, total;
   __host__ __device__ PfSmem() {
     int o = 0;
     b = o; o += PF_NB_ST * PF_STAGE_B;                          // 1024-aligned (dynamic smem base)
-    bars = o; o += 8 * (2 * PF_NB_ST + 2 * PF_NA_ST + 4 + 1);
+    raw = o; o += PF_NR_ST * PF_RAW_STAGE;                      // 1024-aligned
+    bars = o; o += 8 * (2 * PF_NB_ST + 2 * PF_NA_ST + 2 * PF_NR_ST + 4 + 1);
     o = (o + 15) & ~15;
     xbuf = o; o += 2 * 32 * 33 * 4;
     tmem = o; o += 16;
@@ -306,19 +386,25 @@ struct PfSmem {
 // CL == 2: clusters of two CTAs sharing each token stage (multicast); CL == 1: alone.
 template <int EPI, int CL>
 __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __grid_constant__ CUtensorMap bmap,
+                                                                     const __grid_constant__ CUtensorMap qmap,
+                                                                     const __grid_constant__ CUtensorMap smap,
                                                                      GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const PfSmem L;
   uint8_t* sb = smem + L.b;
+  uint8_t* sraw = smem + L.raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* b_full = bars;
-  uint64_t* b_empty = b_full + PF_NB_ST;
-  uint64_t* a_full = b_empty + PF_NB_ST;
-  uint64_t* a_empty = a_full + PF_NA_ST;
-  uint64_t* d_full = a_empty + PF_NA_ST;
+  // k-step kc uses A stage and B stage kc % PF_NA_ST; one MMA commit per
+  // k-step releases both (with CL == 2, in both CTAs of the pair)
+  uint64_t* ab_empty = b_full + PF_NB_ST;
+  uint64_t* a_full = ab_empty + PF_NB_ST;
+  uint64_t* d_full = a_full + PF_NA_ST + PF_NA_ST;
   uint64_t* d_empty = d_full + 2;
   uint64_t* done_bar = d_empty + 2;
+  uint64_t* r_full = done_bar + 1;
+  uint64_t* r_empty = r_full + PF_NR_ST;
   float* xbuf = reinterpret_cast<float*>(smem + L.xbuf);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.tmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
@@ -327,20 +413,25 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   if (threadIdx.x == 0) {
     for (int i = 0; i < PF_NB_ST; ++i) {
       mbar_init(&b_full[i], 1);
-      mbar_init(&b_empty[i], CL);  // the MMAs of every CTA of the cluster
+      mbar_init(&ab_empty[i], CL);  // the MMAs of every CTA of the cluster
     }
     for (int i = 0; i < PF_NA_ST; ++i) {
-      mbar_init(&a_full[i], PF_DQ_WARPS * 32);
-      mbar_init(&a_empty[i], 1);
+      mbar_init(&a_full[i], PF_DQ_WARPS);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&d_full[i], 1);
       mbar_init(&d_empty[i], 128);
     }
     mbar_init(done_bar, 1);
+    for (int i = 0; i < PF_NR_ST; ++i) {
+      mbar_init(&r_full[i], 1);
+      mbar_init(&r_empty[i], PF_DQ_WARPS);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&bmap);
+    tma_prefetch_desc(&qmap);
+    tma_prefetch_desc(&smap);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, 512);
@@ -366,12 +457,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
     // ------------------------------------------------ B producer (TMA)
     if (lane == 0) {
       int kc = 0;
+      int4 nxt = t0 < ntiles ? a.tiles[t0] : make_int4(0, 0, 0, 0);
       for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
-        const int4 tile = a.tiles[t];
+        const int4 tile = nxt;
+        if (t + tstep < ntiles) nxt = a.tiles[t + tstep];  // read one tile ahead
         const int nbox = (tile.w + PF_BOXR - 1) / PF_BOXR;
         for (int ks = 0; ks < KS; ++ks, ++kc) {
           const int s = kc % PF_NB_ST;
-          if (kc >= PF_NB_ST && !mbar_wait(&b_empty[s], ((kc / PF_NB_ST) - 1) & 1, abort_flag)) {
+          if (kc >= PF_NB_ST && !mbar_wait(&ab_empty[s], ((kc / PF_NB_ST) - 1) & 1, abort_flag)) {
             *abort_flag = 1;
             flag_status(a.status, DEV_TIMEOUT_MMA);
             break;
@@ -398,8 +491,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
     if (lane == 0) {
       int kc = 0, ti = 0;
       bool issued_any = false;
+      int4 nxt = t0 < ntiles ? a.tiles[t0] : make_int4(0, 0, 0, 0);
       for (int t = t0; t < ntiles && !*abort_flag; t += tstep, ++ti) {
-        const int4 tile = a.tiles[t];
+        const int4 tile = nxt;
+        if (t + tstep < ntiles) nxt = a.tiles[t + tstep];
         const int ab = ti & 1;
         if (ti >= 2 && !mbar_wait(&d_empty[ab], ((ti >> 1) - 1) & 1, abort_flag)) {
           *abort_flag = 1;
@@ -425,11 +520,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
                        (ks | kk) != 0);
           }
           issued_any = true;
-          mma_commit(&a_empty[sa]);
           if (CL == 2)
-            mma_commit_mc(&b_empty[sbk], 0x3);  // both CTAs' B stage is refilled once both MMAs are done
+            mma_commit_mc(&ab_empty[sa], 0x3);  // the shared B stage is refilled once both MMAs are done
           else
-            mma_commit(&b_empty[sbk]);
+            mma_commit(&ab_empty[sa]);
         }
         if (*abort_flag) break;
         mma_commit(&d_full[ab]);
@@ -440,68 +534,100 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
         mbar_wait(done_bar, 0, nullptr);
       }
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------ A producer (TMA of the raw weight bytes)
+    if (lane == 0) {
+      int rc = 0;
+      const int ngroups = (KS + PF_RAW_KS - 1) / PF_RAW_KS;
+      int4 nxt = t0 < ntiles ? a.tiles[t0] : make_int4(0, 0, 0, 0);
+      for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
+        const int4 tile = nxt;
+        if (t + tstep < ntiles) nxt = a.tiles[t + tstep];  // read one tile ahead
+        const int64_t base = static_cast<int64_t>(tile.x) * a.rows_per_expert;
+        // weight rows of A rows 0..63 and 64..127: gate and up features (GEMM 1) or 128 outputs (GEMM 2)
+        const int y0 = static_cast<int>(EPI == 1 ? base + tile.y * 64 : base + tile.y * 128);
+        const int y1 = static_cast<int>(EPI == 1 ? base + a.I + tile.y * 64 : base + tile.y * 128 + 64);
+        for (int g = 0; g < ngroups; ++g, ++rc) {
+          const int r = rc % PF_NR_ST;
+          if (rc >= PF_NR_ST && !mbar_wait(&r_empty[r], ((rc / PF_NR_ST) - 1) & 1, abort_flag)) {
+            *abort_flag = 1;
+            flag_status(a.status, DEV_TIMEOUT_PIPE);
+            break;
+          }
+          uint8_t* st = sraw + r * PF_RAW_STAGE;
+          mbar_arrive_expect_tx(&r_full[r], PF_RAW_STAGE);
+          tma_load_2d(st, &qmap, g * 128, y0, &r_full[r]);
+          tma_load_2d(st + 64 * 128, &qmap, g * 128, y1, &r_full[r]);
+          tma_load_2d(st + PF_RAW_QS, &smap, g * 16, y0, &r_full[r]);
+          tma_load_2d(st + PF_RAW_QS + 64 * 16, &smap, g * 16, y1, &r_full[r]);
+        }
+      }
+      if (*abort_flag) {
+        for (int j = rc - 1; j >= 0 && j >= rc - PF_NR_ST; --j)
+          mbar_wait(&r_full[j % PF_NR_ST], (j / PF_NR_ST) & 1, nullptr);
+      }
+    }
   } else if (warp < PF_EPI0) {
-    // ------------------------------------------------ A producers: dequantise into TMEM
+    // ------------------------------------------------ dequantise into TMEM
     // warp pair (w, w + 4) shares lane quarter q; half h dequantises block h
     // of each 64-input k-step (TMEM columns 16h .. 16h+15 of the stage).
     const int q = warp & 3;
-    const int h = (warp - 2) >> 2;
+    const int h = (warp - PF_DQ0) >> 2;
     const int m = 32 * q + lane;  // A row = TMEM lane
-    constexpr int PD = 3;         // k-steps of raw bytes in flight per thread
-    int kc = 0;
+    // this row's bytes in a raw stage: 128-byte rows, 16-byte chunk c stored at chunk c ^ (row & 7)
+    const int qoff = (m >> 6) * 64 * 128 + (m & 63) * 128;
+    const int soff = PF_RAW_QS + (m >> 6) * 64 * 16 + (m & 63) * 16;
+    const int ngroups = (KS + PF_RAW_KS - 1) / PF_RAW_KS;
+    int kc = 0, rc = 0;
     for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
-      const int4 tile = a.tiles[t];
-      int64_t row;
-      if (EPI == 1) {
-        const int64_t base = static_cast<int64_t>(tile.x) * a.rows_per_expert;
-        row = m < 64 ? base + tile.y * 64 + m : base + a.I + tile.y * 64 + (m - 64);
-      } else {
-        row = static_cast<int64_t>(tile.x) * a.rows_per_expert + tile.y * 128 + m;
-      }
-      const uint8_t* qp = a.qs + row * a.qrow + 16 * h;
-      const uint16_t* sp = reinterpret_cast<const uint16_t*>(a.sc + row * a.scrow) + h;
-      uint4 rq[PD];
-      uint16_t rs[PD];
-#pragma unroll
-      for (int i = 0; i < PD; ++i) {
-        if (i < KS) {
-          rq[i] = ldg_nc_v4(qp + i * 32);
-          rs[i] = __ldg(sp + 2 * i);
-        }
-      }
-      for (int ks = 0; ks < KS; ++ks, ++kc) {
-        const uint4 cq = rq[0];
-        const uint16_t cs = rs[0];
-#pragma unroll
-        for (int i = 0; i + 1 < PD; ++i) {
-          rq[i] = rq[i + 1];
-          rs[i] = rs[i + 1];
-        }
-        if (ks + PD < KS) {
-          rq[PD - 1] = ldg_nc_v4(qp + (ks + PD) * 32);
-          rs[PD - 1] = __ldg(sp + 2 * (ks + PD));
-        }
-        uint32_t col[16];
-        dequant_block16(cq, cs, col);
-        const int s = kc % PF_NA_ST;
-        if (kc >= PF_NA_ST && !mbar_wait(&a_empty[s], ((kc / PF_NA_ST) - 1) & 1, abort_flag)) {
+      for (int g = 0; g < ngroups && !*abort_flag; ++g, ++rc) {
+        const int r = rc % PF_NR_ST;
+        if (!mbar_wait(&r_full[r], (rc / PF_NR_ST) & 1, abort_flag)) {
           *abort_flag = 1;
-          flag_status(a.status, DEV_TIMEOUT_MMA);
+          flag_status(a.status, DEV_TIMEOUT_PIPE);
           break;
         }
-        tc_fence_after();
-        tmem_st16(tmem + (static_cast<uint32_t>(32 * q) << 16) + PF_ACOL + s * 32 + 16 * h, col);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&a_full[s]);
+        const uint8_t* st = sraw + r * PF_RAW_STAGE;
+        const int nk = min(PF_RAW_KS, KS - g * PF_RAW_KS);
+        const uint4 scv = *reinterpret_cast<const uint4*>(st + soff);
+        uint4 qv[PF_RAW_KS];
+#pragma unroll
+        for (int j = 0; j < PF_RAW_KS; ++j)
+          if (j < nk) qv[j] = *reinterpret_cast<const uint4*>(st + qoff + (((2 * j + h) ^ (m & 7)) << 4));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&r_empty[r]);  // the raw bytes are in registers
+        const uint32_t sw[4] = {scv.x, scv.y, scv.z, scv.w};
+#pragma unroll
+        for (int j = 0; j < PF_RAW_KS; ++j) {
+          if (j >= nk) break;
+          // scale of block 2j + h of the group: 16-bit half h of word j
+          const uint16_t dbits = static_cast<uint16_t>(h ? (sw[j] >> 16) : (sw[j] & 0xFFFFu));
+          uint32_t col[16];
+          dequant_block16(qv[j], dbits, col);
+          const int s = kc % PF_NA_ST;
+          if (kc >= PF_NA_ST && !mbar_wait(&ab_empty[s], ((kc / PF_NA_ST) - 1) & 1, abort_flag)) {
+            *abort_flag = 1;
+            flag_status(a.status, DEV_TIMEOUT_MMA);
+            break;
+          }
+          tc_fence_after();
+          tmem_st16(tmem + (static_cast<uint32_t>(32 * q) << 16) + PF_ACOL + s * 32 + 16 * h, col);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[s]);  // the warp's 32 rows of this block are in TMEM
+          ++kc;
+        }
       }
     }
   } else {
     // ------------------------------------------------ epilogue
     const int q = warp & 3;
     int ti = 0;
+    int4 nxt = t0 < ntiles ? a.tiles[t0] : make_int4(0, 0, 0, 0);
     for (int t = t0; t < ntiles; t += tstep, ++ti) {
-      const int4 tile = a.tiles[t];
+      const int4 tile = nxt;
+      if (t + tstep < ntiles) nxt = a.tiles[t + tstep];
       const int ab = ti & 1;
       bool stop = *abort_flag != 0;
       if (!stop && !mbar_wait(&d_full[ab], (ti >> 1) & 1, abort_flag)) {
@@ -599,9 +725,32 @@ bool make_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D byte map over a weight plane: [rows][pitch] with `used` bytes a row,
+// box box_x bytes x 64 rows.
+bool make_plane_map(CUtensorMap* m, const void* base, int64_t rows, int64_t used, int64_t pitch, int box_x,
+                    CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(used), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_x), 64};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Nibble map (box 128 bytes = 4 k-steps, 128-byte swizzle) and scale map
+// (box 16 bytes = the 8 scales of the same 4 k-steps) of a weight stack.
+bool make_weight_maps(CUtensorMap* qm, CUtensorMap* sm, const moex_qweight* w) {
+  const int64_t rows = static_cast<int64_t>(w->n_mats) * w->rows;
+  return make_plane_map(qm, w->qs, rows, w->K / 2, qs_row_bytes(w->fmt, w->K), 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_plane_map(sm, w->scales, rows, w->K / 16, sc_row_bytes(w->K), 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-using PfKernel = void (*)(CUtensorMap, GemmArgs);
+using PfKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, GemmArgs);
 
 cudaLaunchConfig_t pf_config(int grid, size_t smem, cudaStream_t s, int cl, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
@@ -642,11 +791,11 @@ int pf_grid(PfKernel kern, int cl, size_t smem) {
   return cached[slot];
 }
 
-cudaError_t launch_pf_gemm(PfKernel kern, int cl, size_t smem, cudaStream_t s, const CUtensorMap& map,
-                           const GemmArgs& args) {
+cudaError_t launch_pf_gemm(PfKernel kern, int cl, size_t smem, cudaStream_t s, const CUtensorMap& bmap,
+                           const CUtensorMap& qmap, const CUtensorMap& smap, const GemmArgs& args) {
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pf_config(pf_grid(kern, cl, smem), smem, s, cl, attr);
-  return cudaLaunchKernelEx(&cfg, kern, map, args);
+  return cudaLaunchKernelEx(&cfg, kern, bmap, qmap, smap, args);
 }
 
 }  // namespace
@@ -655,13 +804,14 @@ cudaError_t launch_pf_gemm(PfKernel kern, int cl, size_t smem, cudaStream_t s, c
 void prefill_ws_layout(int T, int k, int E, int64_t hidden, int64_t inter, size_t* off) {
   const size_t n = static_cast<size_t>(T) * k;
   const size_t tiles = n / PF_NMAX + E + 1;
+  const size_t segs = static_cast<size_t>(pf_nsegs(static_cast<int>(n)));
   size_t o = 0;
-  off[0] = o; o = align_up(o + 4 * E, 256);                              // counts
+  off[0] = o; o = align_up(o + 4 * E + 4 * segs * E + 8 * E + 4, 256);  // counts, segment histograms, eoff, etb
   off[1] = o; o = align_up(o + 4 * n, 256);                              // order
   off[2] = o; o = align_up(o + 8 * n, 256);                              // tokw
   off[3] = o; o = align_up(o + 16 * tiles * (inter / 64), 256);          // tiles 1
   off[4] = o; o = align_up(o + 16 * tiles * (hidden / 128), 256);        // tiles 2
-  off[5] = o; o = align_up(o + 16, 256);                                 // n1, n2
+  off[5] = o; o = align_up(o + 16, 256);                                 // n1, n2, placed rows
   off[6] = o; o = align_up(o + 2 * n * hidden, 256);                     // Xs
   off[7] = o; o = align_up(o + 2 * n * inter, 256);                      // Hs
   off[8] = o;                                                            // total
@@ -695,16 +845,31 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   __half* hs = reinterpret_cast<__half*>(wsb + off[7]);
   uint32_t* status = device_status_ptr();
 
-  CUtensorMap m1, m2;
-  if (!make_map(&m1, xs, n, H) || !make_map(&m2, hs, n, I)) return MOEX_ECUDA;
+  CUtensorMap m1, m2, q1, s1, q2, s2;
+  if (!make_map(&m1, xs, n, H) || !make_map(&m2, hs, n, I) || !make_weight_maps(&q1, &s1, gu) ||
+      !make_weight_maps(&q2, &s2, dn))
+    return MOEX_ECUDA;
 
-  if (launch_pdl(prefill_count_kernel, dim3(E), dim3(256), 0, s, ids, n, E, counts, status) != cudaSuccess)
+  int* hist = counts + E;
+  const int S = pf_nsegs(n);
+  const size_t esm = static_cast<size_t>(E) * sizeof(int);
+  if (launch_pdl(prefill_hist_kernel, dim3(S), dim3(256), esm, s, ids, n, E, hist, status) != cudaSuccess)
     return MOEX_ECUDA;
-  if (launch_pdl(prefill_place_kernel, dim3(E), dim3(256), 0, s, ids, w, n, k, E, static_cast<const int*>(counts),
-                 order, tokw, tl) != cudaSuccess)
+  int* eoff = hist + static_cast<int64_t>(S) * E;
+  int* etb = eoff + E;
+  if (launch_pdl(prefill_scan_kernel, dim3(1), dim3(1024), 0, s, n, E, hist, counts, eoff, etb, tl) != cudaSuccess)
     return MOEX_ECUDA;
-  if (launch_pdl(prefill_gather_kernel, dim3((n * 32 + 255) / 256), dim3(256), 0, s, x, H, k, n,
-                 static_cast<const int*>(order), xs) != cudaSuccess)
+  const int64_t max_tiles = (static_cast<int64_t>(n) / PF_NMAX + E + 1) * (tl.F1 + tl.F2);
+  if (launch_pdl(prefill_tiles_kernel, dim3(static_cast<unsigned>((max_tiles + 255) / 256)), dim3(256), 0, s, E,
+                 static_cast<const int*>(counts), static_cast<const int*>(eoff), static_cast<const int*>(etb),
+                 tl) != cudaSuccess)
+    return MOEX_ECUDA;
+  if (launch_pdl(prefill_scatter_kernel, dim3(S), dim3(32), esm, s, ids, w, n, k, E, static_cast<const int*>(hist),
+                 order, tokw) != cudaSuccess)
+    return MOEX_ECUDA;
+  const int64_t gthreads = static_cast<int64_t>(n) * (H / 8);
+  if (launch_pdl(prefill_gather_kernel, dim3(static_cast<unsigned>((gthreads + 255) / 256)), dim3(256), 0, s, x, H,
+                 k, static_cast<const int*>(tl.n1 + 2), static_cast<const int*>(order), xs) != cudaSuccess)
     return MOEX_ECUDA;
   const PfSmem L;
   // pairs share each token stage when both GEMMs have an even number of feature tiles
@@ -726,7 +891,7 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   g1.Hs = hs;
   g1.I = I;
   g1.status = status;
-  if (launch_pf_gemm(k1, cl, L.total, s, m1, g1) != cudaSuccess) return MOEX_ECUDA;
+  if (launch_pf_gemm(k1, cl, L.total, s, m1, q1, s1, g1) != cudaSuccess) return MOEX_ECUDA;
   if (cudaMemsetAsync(out, 0, static_cast<size_t>(T) * H * sizeof(float), s) != cudaSuccess) return MOEX_ECUDA;
   GemmArgs g2 = {};
   g2.qs = static_cast<const uint8_t*>(dn->qs);
@@ -741,7 +906,7 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   g2.Hd = H;
   g2.tokw = tokw;
   g2.status = status;
-  if (launch_pf_gemm(k2, cl, L.total, s, m2, g2) != cudaSuccess) return MOEX_ECUDA;
+  if (launch_pf_gemm(k2, cl, L.total, s, m2, q2, s2, g2) != cudaSuccess) return MOEX_ECUDA;
   return MOEX_OK;
 }
 
