@@ -1,9 +1,9 @@
 """Benchmark of the block-quantized decode GEMV path on GB300.
 
 Headline workload: Q8_0 weights 8192 x 2560 against q8_1 activations; one
-step = for ncols in (1, 2, 4, 8): quantize_q8_1 of the FP32 columns, then the
-multi-column GEMV, each on the next of enough rotated weight copies that the
-weights are cold (3x L2).  value = weight GB/s over the timed steps (bytes of
+step = quantize_q8_1 of the step's 15 FP32 columns (one launch), then the
+multi-column GEMV for ncols 1, 2, 4 and 8, each on the next of enough rotated
+weight copies that the weights are cold (3x L2).  value = weight GB/s over the timed steps (bytes of
 the four GEMVs / time); the per-column-count microseconds per call, the
 IQ4_NL 12288 x 2560 GEMV and the grouped MoE decode layer are reported in
 "detail".
@@ -163,20 +163,28 @@ class GemvCase:
             w.qs.copy_(w0.qs)
             w.scales.copy_(w0.scales)
             self.W.append(w)
+        # the activations of every column count of a step, stacked so one
+        # quantize_q8_1 call covers the step; x[c], xq[c], xds[c] are views
+        ntot = sum(ncols_list)
+        self.x_all = torch.empty((ntot, k), dtype=torch.float32, device="cuda")
+        self.xq_all = torch.empty((ntot, k), dtype=torch.int8, device="cuda")
+        self.xds_all = torch.empty((ntot, k // 32, 2), dtype=torch.float32, device="cuda")
         self.x, self.xq, self.xds, self.y = {}, {}, {}, {}
+        o = 0
         for c in ncols_list:
-            xs = synth.activations(synth.rng(100 + c), c, k)
-            self.x[c] = torch.from_numpy(xs).cuda()
-            self.xq[c] = torch.empty((c, k), dtype=torch.int8, device="cuda")
-            self.xds[c] = torch.empty((c, k // 32, 2), dtype=torch.float32, device="cuda")
+            self.x_all[o:o + c].copy_(torch.from_numpy(synth.activations(synth.rng(100 + c), c, k)))
+            self.x[c], self.xq[c], self.xds[c] = self.x_all[o:o + c], self.xq_all[o:o + c], self.xds_all[o:o + c]
             self.y[c] = torch.empty((c, rows), dtype=torch.float32, device="cuda")
+            o += c
 
     def step(self, i, ncols_list, quantize=True):
+        """One step: q8_1 of all the step's columns (one launch), then the
+        GEMV of each column count on the next cold weight copy."""
         import moe_expert_gb300 as mx
+        if quantize:
+            mx.quantize_q8_1(self.x_all, self.xq_all, self.xds_all)
         for j, c in enumerate(ncols_list):
             w = self.W[(i * len(ncols_list) + j) % self.ncopies]
-            if quantize:
-                mx.quantize_q8_1(self.x[c], self.xq[c], self.xds[c])
             mx.qgemv(w, self.xq[c], self.xds[c], self.y[c])
 
 
@@ -281,12 +289,14 @@ def decode_layer_detail(reps, copies=3):
             "weight_bytes": wbytes, "weight_GBps": round(wbytes / (t2 / reps) / 1e9, 1)}
 
 
-def prefill_layer_detail(reps=5, peak_tflops=None):
-    """Grouped MoE prefill layer: 8192 tokens x top-8 of 128 IQ4_NL experts,
-    hidden 2560, inter 1536 (route + sort + gather + two tcgen05 GEMMs)."""
+def prefill_layer_detail(reps=5, peak_tflops=None, T=8192, E=128):
+    """Grouped MoE prefill layer: T tokens x top-8 of E IQ4_NL experts,
+    hidden 2560, inter 1536 (route + sort + gather + two tcgen05 GEMMs).
+    The workload is 8192 tokens over 128 experts; 4096 over 64 keeps the
+    same rows per expert at half the memory (the profiler's case)."""
     import torch
     import moe_expert_gb300 as mx
-    T, E, k, hidden, inter = 8192, 128, 8, 2560, 1536
+    k, hidden, inter = 8, 2560, 1536
     gu = mx.PackedWeight("iq4_nl", E, 2 * inter, hidden)
     dn = mx.PackedWeight("iq4_nl", E, hidden, inter)
     for e in range(E):
@@ -320,6 +330,38 @@ def prefill_layer_detail(reps=5, peak_tflops=None):
     return d
 
 
+GEMV_SOURCES = ("moe_expert_gb300/csrc/qgemv.cu", "moe_expert_gb300/csrc/gemv_core.cuh",
+                "moe_expert_gb300/csrc/common.cuh")
+
+
+def sources_digest(paths):
+    import hashlib
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name, sources):
+    """DRAM bytes per launch of the dominant kernel from its ncu summary in
+    profiles/ (lines 'dram_bytes_per_launch: N' and 'sources_sha256_16: H');
+    None when the kernel sources changed since that capture."""
+    p = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if ":" in line:
+            key, _, v = line.partition(":")
+            vals[key.strip().lstrip("-* ")] = v.strip().strip("`")
+    if vals.get("sources_sha256_16") != sources_digest(sources):
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
 def run_ours(args, ws, rank, local):
     import torch
     import moe_expert_gb300 as mx
@@ -329,19 +371,31 @@ def run_ours(args, ws, rank, local):
     l2 = getattr(props, "L2_cache_size", 126 * 2**20) or 126 * 2**20
     peak, peak_src = peaks()
     case = GemvCase("q8_0", ROWS, K, NCOLS, l2)
-    nsteps_graph = case.ncopies  # one graph per rotation position
-    gs = graphs_for(lambda i: case.step(i, NCOLS), nsteps_graph)
+    # one graph per rotation position (single steps) and one graph of a whole
+    # rotation (G consecutive steps), so graph launches do not pace the GPU
+    G = case.ncopies
+    gs = graphs_for(lambda i: case.step(i, NCOLS), G)
+    cycle = graphs_for(lambda _: [case.step(i, NCOLS) for i in range(G)], 1)[0]
+
+    def run_steps(first, count):
+        """Steps first .. first+count-1 (rotation position = step mod G)."""
+        i = first
+        while i < first + count:
+            if i % G == 0 and first + count - i >= G:
+                cycle.replay()
+                i += G
+            else:
+                gs[i % G].replay()
+                i += 1
     # warm-up + timed steps (device time, CUDA events), clocks sampled meanwhile
-    for i in range(args.warmup):
-        gs[i % len(gs)].replay()
+    run_steps(0, args.warmup)
     torch.cuda.synchronize()
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for i in range(args.steps):
-            gs[(args.warmup + i) % len(gs)].replay()
+        run_steps(args.warmup, args.steps)
         e1.record()
         torch.cuda.synchronize()
     barrier(ws)
@@ -358,21 +412,18 @@ def run_ours(args, ws, rank, local):
         kt += kern[c]
     avg_launch = kt / len(NCOLS)
     achieved = W_BYTES / avg_launch / 1e9
-    traffic = None
-    tp = os.path.join(ROOT, "profiles", "qgemv_q8_0_8192x2560_traffic.json")
-    if os.path.exists(tp):
-        traffic = json.load(open(tp)).get("bytes_per_launch")
+    traffic = profiled_traffic("qgemv_q8_0_8192x2560.md", GEMV_SOURCES)
 
     # end to end through the public API: pinned host X in, host Y out, eager calls
-    xs_h = {c: case.x[c].cpu().pin_memory() for c in NCOLS}
+    xs_h = case.x_all.cpu().pin_memory()
     ys_h = {c: torch.empty((c, ROWS), dtype=torch.float32).pin_memory() for c in NCOLS}
     e2e_steps = max(50, min(args.steps, 2000))
 
     def e2e_step(i):
+        case.x_all.copy_(xs_h, non_blocking=True)
+        mx.quantize_q8_1(case.x_all, case.xq_all, case.xds_all)
         for j, c in enumerate(NCOLS):
             w = case.W[(i * len(NCOLS) + j) % case.ncopies]
-            case.x[c].copy_(xs_h[c], non_blocking=True)
-            mx.quantize_q8_1(case.x[c], case.xq[c], case.xds[c])
             mx.qgemv(w, case.xq[c], case.xds[c], case.y[c])
             ys_h[c].copy_(case.y[c], non_blocking=True)
     for i in range(min(args.warmup, 20)):
@@ -391,7 +442,7 @@ def run_ours(args, ws, rank, local):
     detail = {}
     if rank == 0 and not args.no_detail:
         detail["q8_0_8192x2560"] = gemv_detail(case, NCOLS, 2000, peak)
-        del case, gs
+        del case, gs, cycle
         torch.cuda.empty_cache()
         iq = GemvCase("iq4_nl", 12288, K, (1, 2, 3, 4, 8), l2)
         for c in (1, 2, 3, 4, 8):
@@ -416,11 +467,12 @@ def run_ours(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8", "data": "synthetic",
         "config": {"workload": "Q8_0 decode GEMV 8192x2560 x q8_1 activations, ncols 1/2/4/8 per step "
-                               "(quantize_q8_1 + qgemv each), cold weights",
+                               "(one quantize_q8_1 of the step's 15 columns, then a qgemv per column count), "
+                               "cold weights",
                    "rows": ROWS, "K": K, "ncols": list(NCOLS), "weight_copies": case_copies(l2),
                    "l2": "inputs larger than L2: rotated weight copies totalling 3x L2",
                    "parallelism": f"replicas x{ws}"},
-        "gpu_launches": args.steps * 2 * len(NCOLS),
+        "gpu_launches": args.steps * (1 + len(NCOLS)),
         "clocks": clk.summary(),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -531,7 +583,7 @@ def run_only(args):
         mx.quantize_q8_1(case.x[c], case.xq[c], case.xds[c])
         fn = lambda i: mx.qgemv(case.W[i % case.ncopies], case.xq[c], case.xds[c], case.y[c])  # noqa: E731
     elif args.only == "prefill":
-        d = prefill_layer_detail(max(1, args.steps), peak_fp16())
+        d = prefill_layer_detail(max(1, args.steps), peak_fp16(), args.pf_tokens, args.pf_experts)
         print(json.dumps({"only": "prefill", **d}))
         return
     elif args.only == "decode":
@@ -562,6 +614,8 @@ def main():
     ap.add_argument("--no-detail", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--pf-tokens", type=int, default=8192, help="--only prefill: tokens")
+    ap.add_argument("--pf-experts", type=int, default=128, help="--only prefill: experts")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -45,14 +45,16 @@ struct GemvSmem {
   }
 };
 
-// Threads of a dense ring GEMV CTA: NS*WPS consumer warps + 1 producer warp.
+// Threads of a dense ring GEMV CTA: NS*WPS*CS consumer warps + 1 producer
+// warp (CS column groups, each warp computing C/CS of the columns).
 // MINB == 2 variants keep registers and shared memory small enough that a
 // CTA of the next GEMV in the stream can be resident beside this one, so
 // with programmatic dependent launch its weight stream starts while this
 // one drains.
-template <int WPS, int MINB>
+template <int WPS, int MINB, int CS>
 struct GemvBounds {
-  static constexpr int MAXT = MINB == 2 ? (5 * WPS + 1) * 32 : 512;
+  static constexpr int MAXT = MINB == 2 ? (5 * WPS * CS + 1) * 32
+                                        : ((5 * WPS * CS + 1) * 32 > 512 ? (5 * WPS * CS + 1) * 32 : 512);
 };
 
 // Ring variant: every CTA owns a contiguous range of rows; one producer
@@ -63,11 +65,13 @@ struct GemvBounds {
 // over the half warp into a per-chunk buffer; every GEMV_CHUNK stages the
 // consumers meet at a barrier and sum over the K slices (no per-stage
 // hand-off between warps).
-template <int FMT, int C, int WPS, int MINB>
-__global__ void __launch_bounds__(GemvBounds<WPS, MINB>::MAXT, MINB) qgemv_kernel(GemvArgs a) {
+template <int FMT, int C, int WPS, int MINB, int CS>
+__global__ void __launch_bounds__(GemvBounds<WPS, MINB, CS>::MAXT, MINB) qgemv_kernel(GemvArgs a) {
+  static_assert(C % CS == 0, "column groups split the columns evenly");
+  constexpr int CG = C / CS;  // columns of one consumer warp
   extern __shared__ __align__(1024) uint8_t smem[];
   MOEX_TRACE_BEGIN();
-  const int nwc = a.NS * WPS;
+  const int nwc = a.NS * WPS * CS;
   const int slot_bytes = a.stage_bytes;
   const GemvSmem L(C, a.NS, a.nst, slot_bytes);
   TmaRing R;
@@ -126,22 +130,23 @@ __global__ void __launch_bounds__(GemvBounds<WPS, MINB>::MAXT, MINB) qgemv_kerne
     return;
   }
 
-  const ConsumerPos pos = consumer_pos(warp, lane, WPS);
+  const int cg = warp / (a.NS * WPS);  // column group: columns cg*CG .. cg*CG+CG-1
+  const ConsumerPos pos = consumer_pos(warp % (a.NS * WPS), lane, WPS);
   pdl_wait();  // activations come from the previous kernel
   MOEX_TRACE_STAMP(1);
-  ActRegs<FMT, C> act;
+  ActRegs<FMT, CG> act;
   {
-    const int8_t* xcol[C];
-    const float* dcol[C];
+    const int8_t* xcol[CG];
+    const float* dcol[CG];
 #pragma unroll
-    for (int c = 0; c < C; ++c) {
-      xcol[c] = a.xq + static_cast<int64_t>(c) * a.K;
-      dcol[c] = a.xds + static_cast<int64_t>(c) * a.NB * 2;
+    for (int c = 0; c < CG; ++c) {
+      xcol[c] = a.xq + static_cast<int64_t>(cg * CG + c) * a.K;
+      dcol[c] = a.xds + static_cast<int64_t>(cg * CG + c) * a.NB * 2;
     }
     const int b = pos.ks * SLICE + pos.li;
-    load_act<FMT, C>(act, xcol, dcol, b, b < a.NB, pos.li, 2);
+    load_act<FMT, CG>(act, xcol, dcol, b, b < a.NB, pos.li, 2);
   }
-  constexpr int N = Vals<C, WPS>::N;
+  constexpr int N = Vals<CG, WPS>::N;
   const int nthr = nwc * 32;
   bool dead = false;
   for (int c0 = 0; c0 < nstage; c0 += GEMV_CHUNK) {
@@ -149,7 +154,7 @@ __global__ void __launch_bounds__(GemvBounds<WPS, MINB>::MAXT, MINB) qgemv_kerne
     for (int it = c0; it < c1 && !dead; ++it) {
       const int n = stage_rows(it);
       float v[N];
-      if (!tma_ring_partials<FMT, C, WPS, N>(R, it, pos, n, a.NB, act, v, abort_flag)) {
+      if (!tma_ring_partials<FMT, CG, WPS, N>(R, it, pos, n, a.NB, act, v, abort_flag)) {
         if (lane == 0) {
           *abort_flag = 1;
           flag_status(a.status, DEV_TIMEOUT_PIPE);
@@ -157,7 +162,9 @@ __global__ void __launch_bounds__(GemvBounds<WPS, MINB>::MAXT, MINB) qgemv_kerne
         dead = true;
         break;
       }
-      reduce_to_red<C, WPS, N>(v, pos, n, a.NS, red + (it - c0) * (SR * a.NS * C));
+      float* rs = red + (it - c0) * (SR * a.NS * C);
+      const int NS = a.NS;
+      reduce_out<CG, WPS, N>(v, pos, n, [&](int row, int c, float val) { rs[(row * NS + pos.ks) * C + cg * CG + c] = val; });
       tma_ring_release(R, it, lane);
     }
     named_bar_sync(1, nthr);
@@ -177,19 +184,23 @@ __global__ void __launch_bounds__(GemvBounds<WPS, MINB>::MAXT, MINB) qgemv_kerne
 
 // ----------------------------------------------------------------- register-staged GEMV
 
-// Small-column variant: every lane loads all of its CTA's weight bytes into
-// registers at entry (plain 16-byte ld.global.nc), before
-// griddepcontrol.wait, so a CTA's whole share of HBM reads is in flight while
-// the previous kernel finishes; nothing of it waits for ring slots or the
-// TMA unit.  Four warps per K slice, one row per half warp per 8-row stage.
-// Partial sums are reduced over the half warp and then over the slices, in
-// slice order, exactly as in the ring variant (same tree: same bits).
+// Small-column variant: every lane streams its CTA's weight bytes through
+// registers with plain 16-byte ld.global.nc, P stages ahead; the first P
+// stages are issued before griddepcontrol.wait, so they are in flight while
+// the previous kernel finishes; nothing waits for ring slots or the TMA
+// unit.  With MINB == 2 the kernel fits in half an SM (<= 48 registers a
+// thread), so the next GEMV in the stream is resident beside it and its
+// first stages load while this one drains.  Four warps per K slice, one row
+// per half warp per 8-row stage.  Partial sums are reduced over the half
+// warp and then over the slices, in slice order, exactly as in the ring
+// variant (same tree: same bits).
 constexpr int REG_WPS = 4;
 
-template <int FMT, int C, int NSTG>
-__global__ void __launch_bounds__(640, 1) qgemv_reg_kernel(GemvArgs a) {
+template <int FMT, int C, int NSTG, int P, int MINB>
+__global__ void __launch_bounds__(640, MINB) qgemv_reg_kernel(GemvArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   float* red = reinterpret_cast<float*>(smem);  // [NSTG*8 rows][NS][C]
+  constexpr int QB16 = FmtTraits<FMT>::QBYTES / 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ConsumerPos pos = consumer_pos(warp, lane, REG_WPS);
   const int64_t G = gridDim.x;
@@ -200,27 +211,29 @@ __global__ void __launch_bounds__(640, 1) qgemv_reg_kernel(GemvArgs a) {
   const bool bvalid = b < a.NB;
   const int my_row0 = pos.jw * 2 + pos.hf;  // row within each stage
 
-  uint4 q[NSTG][FmtTraits<FMT>::QBYTES / 16];
-  uint32_t sw[NSTG];
-#pragma unroll
-  for (int st = 0; st < NSTG; ++st) {
+  uint4 q[P][QB16];
+  uint32_t sw[P];
+  auto load_stage = [&](int st, int slot) {
     const int row = st * SR + my_row0;
     if (bvalid && row < nrows) {
       const uint8_t* src = a.qs + (row_begin + row) * a.qrow + b * FmtTraits<FMT>::QBYTES;
 #pragma unroll
-      for (int h = 0; h < FmtTraits<FMT>::QBYTES / 16; ++h)
+      for (int h = 0; h < QB16; ++h)
         asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(q[st][h].x), "=r"(q[st][h].y), "=r"(q[st][h].z), "=r"(q[st][h].w)
+                     : "=r"(q[slot][h].x), "=r"(q[slot][h].y), "=r"(q[slot][h].z), "=r"(q[slot][h].w)
                      : "l"(src + 16 * h));
       asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];"
-                   : "=r"(sw[st])
+                   : "=r"(sw[slot])
                    : "l"(a.sc + (row_begin + row) * a.scrow + 4 * (b >> 1)));
     } else {
 #pragma unroll
-      for (int h = 0; h < FmtTraits<FMT>::QBYTES / 16; ++h) q[st][h] = make_uint4(0, 0, 0, 0);
-      sw[st] = 0;
+      for (int h = 0; h < QB16; ++h) q[slot][h] = make_uint4(0, 0, 0, 0);
+      sw[slot] = 0;
     }
-  }
+  };
+#pragma unroll
+  for (int st = 0; st < P; ++st)
+    if (st < NSTG) load_stage(st, st);
   pdl_launch_dependents();
   pdl_wait();  // activations come from the previous kernel
   ActRegs<FMT, C> act;
@@ -237,14 +250,16 @@ __global__ void __launch_bounds__(640, 1) qgemv_reg_kernel(GemvArgs a) {
   constexpr int N = pow2_ceil(C);
 #pragma unroll
   for (int st = 0; st < NSTG; ++st) {
+    const int slot = st % P;
     const int row = st * SR + my_row0;
     float v[N];
 #pragma unroll
     for (int i = 0; i < N; ++i) v[i] = 0.f;
     if (bvalid && row < nrows) {
-      const uint16_t hb = static_cast<uint16_t>((b & 1) ? (sw[st] >> 16) : (sw[st] & 0xFFFFu));
-      block_dots_from<FMT, C>(q[st][0], q[st][FmtTraits<FMT>::QBYTES / 16 - 1], __half2float(__ushort_as_half(hb)), act, v);
+      const uint16_t hb = static_cast<uint16_t>((b & 1) ? (sw[slot] >> 16) : (sw[slot] & 0xFFFFu));
+      block_dots_from<FMT, C>(q[slot][0], q[slot][QB16 - 1], __half2float(__ushort_as_half(hb)), act, v);
     }
+    if (st + P < NSTG) load_stage(st + P, slot);  // refill the slot just consumed
     halving_reduce<N, 8>(v, lane);
     // lane li holds value li / (16/N) (N < 16 always here)
     constexpr int REP = 16 / N;
@@ -286,10 +301,10 @@ __global__ void block_dots_kernel(const uint8_t* __restrict__ qs, int64_t rows, 
 
 namespace {
 
-template <int FMT, int C, int WPS, int MINB>
+template <int FMT, int C, int WPS, int MINB, int CS = 1>
 moex_status launch_one(const GemvArgs& base, int smem_cap, cudaStream_t s) {
   GemvArgs a = base;
-  auto kern = qgemv_kernel<FMT, C, WPS, MINB>;
+  auto kern = qgemv_kernel<FMT, C, WPS, MINB, CS>;
   // ring slots: as many as fit the budget (two CTAs per SM for MINB == 2), at most 8
   const int budget = MINB == 2 ? 110 * 1024 : smem_cap;
   const int slot_bytes = ((SR * (a.qrow + a.scrow)) + 127) & ~127;
@@ -303,16 +318,16 @@ moex_status launch_one(const GemvArgs& base, int smem_cap, cudaStream_t s) {
   if (ensure_smem(reinterpret_cast<const void*>(kern), L.total) != cudaSuccess) return MOEX_ECUDA;
   const int64_t max_ctas = (a.rows + SR - 1) / SR;
   const int grid = static_cast<int>(max_ctas < sm_count() ? max_ctas : sm_count());
-  const int threads = (a.NS * WPS + 1) * 32;
+  const int threads = (a.NS * WPS * CS + 1) * 32;
   return cuda_status(launch_pdl(kern, dim3(grid), dim3(threads), L.total, s, a));
 }
 
 // Register-staged variant: K <= 2560 (5 slices x 4 warps = 640 threads), the
 // CTA's rows fit NSTG stages, and the columns are few enough that the
 // weights, scales and activations all fit the register budget.
-template <int FMT, int C, int NSTG>
+template <int FMT, int C, int NSTG, int P, int MINB>
 moex_status launch_reg(const GemvArgs& a, cudaStream_t s) {
-  auto kern = qgemv_reg_kernel<FMT, C, NSTG>;
+  auto kern = qgemv_reg_kernel<FMT, C, NSTG, P, MINB>;
   const int64_t cap_rows = static_cast<int64_t>(SR) * NSTG;
   int64_t grid = sm_count();
   if ((a.rows + grid - 1) / grid > cap_rows) grid = (a.rows + cap_rows - 1) / cap_rows;
@@ -329,12 +344,21 @@ moex_status launch_reg(const GemvArgs& a, cudaStream_t s) {
 template <int FMT, int C>
 moex_status launch_c(const GemvArgs& a, int smem_cap, cudaStream_t s) {
   if constexpr (C <= (FMT == MOEX_IQ4_NL ? 4 : 2)) {
+    // stages ahead and CTAs per SM: the pipelined half-SM form where the
+    // registers allow it, else every stage in flight at once
     constexpr int NSTG = FMT == MOEX_IQ4_NL ? 12 : 8;
-    if (a.NS <= 5 && a.rows <= static_cast<int64_t>(sm_count()) * SR * NSTG * 4) return launch_reg<FMT, C, NSTG>(a, s);
+    constexpr bool HALF = C == 1;
+    constexpr int P = !HALF ? NSTG : FMT == MOEX_Q8_0 ? 3 : 4;
+    if (a.NS <= 5 && a.rows <= static_cast<int64_t>(sm_count()) * SR * NSTG * 4)
+      return launch_reg<FMT, C, NSTG, P, HALF ? 2 : 1>(a, s);
   }
   if (a.NS <= 5) {
+    // up to 4 columns: two warps per slice, two CTAs per SM (the next GEMV
+    // overlaps this one's drain); more columns are compute-bound: one CTA
+    // per SM with twice the warps, the columns split over two warp groups
     if constexpr (C <= 4) return launch_one<FMT, C, 2, 2>(a, smem_cap, s);
-    else return launch_one<FMT, C, 1, 2>(a, smem_cap, s);
+    else if constexpr (C % 2 == 0) return launch_one<FMT, C, 2, 1, 2>(a, smem_cap, s);
+    else return launch_one<FMT, C, 2, 1>(a, smem_cap, s);
   }
   return launch_one<FMT, C, 1, 1>(a, smem_cap, s);
 }
