@@ -255,33 +255,40 @@ __global__ void __launch_bounds__(32) prefill_scatter_kernel(const int32_t* __re
 // ----------------------------------------------------------------- gather
 
 // Xs[p] = fp16(x[token(order[p])]) with each 32-input block interleaved,
-// for the placed rows p < *nrows.  One thread per 16 output bytes: the
-// pairs (j, j+16) for j = 4c .. 4c+3 of a block, from two 8-byte loads.
+// for the placed rows p < *nrows.  One thread per 32-input block: 64 bytes
+// in, 64 bytes out, all four 16-byte loads issued before any convert.
 __global__ void __launch_bounds__(256) prefill_gather_kernel(const uint16_t* __restrict__ x, int H, int k,
                                                              const int* __restrict__ nrows,
                                                              const int* __restrict__ order, __half* __restrict__ xs) {
   pdl_wait();
   pdl_launch_dependents();
-  const int per_row = H / 8;
+  const int per_row = H / QK;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t row = i / per_row;
   if (row >= *nrows) return;
-  const int c = static_cast<int>(i - row * per_row);
-  const int blk = c >> 2, cc = c & 3;
+  const int blk = static_cast<int>(i - row * per_row);
   const int t = order[row] / k;
-  const uint16_t* src = x + static_cast<int64_t>(t) * H + blk * QK + 4 * cc;
-  const uint2 lo = *reinterpret_cast<const uint2*>(src);        // inputs 4cc .. 4cc+3
-  const uint2 hi = *reinterpret_cast<const uint2*>(src + 16);   // inputs 4cc+16 .. 4cc+19
-  const uint32_t a[4] = {lo.x & 0xFFFFu, lo.x >> 16, lo.y & 0xFFFFu, lo.y >> 16};
-  const uint32_t b[4] = {hi.x & 0xFFFFu, hi.x >> 16, hi.y & 0xFFFFu, hi.y >> 16};
-  uint32_t o[4];
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H + blk * QK);
+  uint32_t in[16];
 #pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    const __half2 h = __halves2half2(__float2half_rn(__uint_as_float(a[jj] << 16)),
-                                     __float2half_rn(__uint_as_float(b[jj] << 16)));
+  for (int j = 0; j < 4; ++j) {
+    const uint4 v = __ldg(src + j);
+    in[4 * j] = v.x; in[4 * j + 1] = v.y; in[4 * j + 2] = v.z; in[4 * j + 3] = v.w;
+  }
+  // element e of the block: 16-bit half (e & 1) of word e >> 1
+  auto elem = [&](int e) -> float {
+    const uint32_t wv = in[e >> 1];
+    return __uint_as_float((e & 1) ? (wv & 0xFFFF0000u) : (wv << 16));
+  };
+  uint32_t o[16];
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj) {
+    const __half2 h = __halves2half2(__float2half_rn(elem(jj)), __float2half_rn(elem(jj + 16)));
     o[jj] = *reinterpret_cast<const uint32_t*>(&h);
   }
-  *reinterpret_cast<uint4*>(xs + row * H + blk * QK + 8 * cc) = make_uint4(o[0], o[1], o[2], o[3]);
+  uint4* dst = reinterpret_cast<uint4*>(xs + row * H + blk * QK);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
 }
 
 // ----------------------------------------------------------------- GEMM
@@ -867,7 +874,7 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   if (launch_pdl(prefill_scatter_kernel, dim3(S), dim3(32), esm, s, ids, w, n, k, E, static_cast<const int*>(hist),
                  order, tokw) != cudaSuccess)
     return MOEX_ECUDA;
-  const int64_t gthreads = static_cast<int64_t>(n) * (H / 8);
+  const int64_t gthreads = static_cast<int64_t>(n) * (H / QK);
   if (launch_pdl(prefill_gather_kernel, dim3(static_cast<unsigned>((gthreads + 255) / 256)), dim3(256), 0, s, x, H,
                  k, static_cast<const int*>(tl.n1 + 2), static_cast<const int*>(order), xs) != cudaSuccess)
     return MOEX_ECUDA;
