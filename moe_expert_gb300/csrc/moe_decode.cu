@@ -452,13 +452,16 @@ __device__ __forceinline__ void dn_group(const DecodeArgs& a, const Groups& G, i
   tma_ring_release(S.R, it0, pos.lane);
 }
 
-template <int FMT, int WPS, int MAXT>
+// TEAMS teams of NS consumer warps (one warp per K slice) take the groups
+// round robin, so several groups are in flight at once: a group is little
+// work behind a long chain of waits, loads and reductions.
+template <int FMT, int TEAMS, int MAXT>
 __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   MOEX_TRACE_BEGIN();
   const int NB = a.I / QK;
   const int NS = num_slices(NB);
-  const int nwc = NS * WPS;
+  const int nwc = NS * TEAMS;
   const int G_ = gridDim.x;
   const int rows_max = (a.H + G_ - 1) / G_;
   const DnSmem L(a.n, a.I, NS, rows_max, a.nst, a.stage_bytes);
@@ -493,7 +496,7 @@ __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.nst; ++i) {
       mbar_init(&S.R.full[i], 1);
-      mbar_init(&S.R.empty[i], nwc);
+      mbar_init(&S.R.empty[i], NS);  // the warps of the team that takes the group
       S.cnt[i] = 0;
     }
     *S.abort_flag = 0;
@@ -539,11 +542,12 @@ __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
     for (int i = threadIdx.x; i < a.n * rows_max * NS; i += nthr) osum[i] = 0.f;
     named_bar_sync(1, nthr);
   }
-  const ConsumerPos pos = consumer_pos(warp, lane, WPS);
+  const int team = warp / NS;
+  const ConsumerPos pos = consumer_pos(warp % NS, lane, 1);
   bool dead = false;
-  for (int g = 0; g < G.ng && !dead; ++g) {
+  for (int g = team; g < G.ng && !dead; g += TEAMS) {
     const int m = G.gstart[g + 1] - G.gstart[g];
-#define MOEX_DN(CC) dn_group<FMT, CC, WPS>(a, G, g, g, nrows, S, pos, hs, hd, osum, rows_max, dead)
+#define MOEX_DN(CC) dn_group<FMT, CC, 1>(a, G, g, g, nrows, S, pos, hs, hd, osum, rows_max, dead)
     switch (m) {
       case 1: MOEX_DN(1); break;
       case 2: MOEX_DN(2); break;
@@ -555,7 +559,7 @@ __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
       default: MOEX_DN(8); break;
     }
 #undef MOEX_DN
-    if (g == 0) MOEX_TRACE_STAMP(2);
+    if (g == team) MOEX_TRACE_STAMP(2);
   }
   MOEX_TRACE_STAMP(3);
   named_bar_sync(1, nthr);
@@ -609,7 +613,7 @@ moex_status launch_gu(const DecodeArgs& base, int smem_cap, cudaStream_t s) {
   return cuda_status(launch_pdl(kern, dim3(grid), dim3(threads), L.total, s, a));
 }
 
-template <int FMT, int WPS, int MAXT>
+template <int FMT, int TEAMS, int MAXT>
 moex_status launch_dn(const DecodeArgs& base, int smem_cap, cudaStream_t s) {
   DecodeArgs a = base;
   const int NB = a.I / QK, NS = num_slices(NB);
@@ -623,9 +627,9 @@ moex_status launch_dn(const DecodeArgs& base, int smem_cap, cudaStream_t s) {
   if (nst < 2) return MOEX_EUNSUPPORTED;
   a.nst = nst;
   const DnSmem L(a.n, a.I, NS, rows_max, nst, slot_bytes);
-  auto kern = moe_dn_kernel<FMT, WPS, MAXT>;
+  auto kern = moe_dn_kernel<FMT, TEAMS, MAXT>;
   if (ensure_smem(reinterpret_cast<const void*>(kern), L.total) != cudaSuccess) return MOEX_ECUDA;
-  const int threads = (NS * WPS + 1) * 32;
+  const int threads = (NS * TEAMS + 1) * 32;
   return cuda_status(launch_pdl(kern, dim3(grid), dim3(threads), L.total, s, a));
 }
 

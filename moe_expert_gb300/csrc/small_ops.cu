@@ -85,8 +85,8 @@ moex_status launch_weight_pack(const moex_qweight* w, const void* blocks, cudaSt
 // logits (larger value first, the lower expert id on ties), then the softmax
 // of the k selected logits with the first (largest) subtracted, summed in
 // slot order.
-constexpr int ROUTE_MAX_PER_LANE = 32;  // E <= 1024
-
+// PER = logits a lane holds (E <= 32 * PER); the host picks the smallest.
+template <int PER>
 __global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int32_t* __restrict__ ids, float* __restrict__ w) {
   pdl_wait();
@@ -95,27 +95,25 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
   const float* row = logits + static_cast<int64_t>(warp) * E;
-  float v[ROUTE_MAX_PER_LANE];
-  const int per = (E + 31) / 32;
+  float v[PER];
 #pragma unroll
-  for (int i = 0; i < ROUTE_MAX_PER_LANE; ++i) {
+  for (int i = 0; i < PER; ++i) {
     const int e = lane + 32 * i;
-    v[i] = (i < per && e < E) ? row[e] : -INFINITY;
+    v[i] = e < E ? row[e] : -INFINITY;
   }
   uint32_t taken = 0;  // bit i: lane's element i selected
-  float sel_v[16];
-  int sel_id[16];
+  float my_v = 0.f;    // lane s keeps the logit and id of selection s
+  int my_id = 0;
   for (int s = 0; s < k; ++s) {
     float best = -INFINITY;
     int bid = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < ROUTE_MAX_PER_LANE; ++i) {
+    for (int i = 0; i < PER; ++i) {
       const int e = lane + 32 * i;
-      if (i < per && e < E && !((taken >> i) & 1u)) {
-        if (v[i] > best || (v[i] == best && e < bid) || bid == 0x7fffffff) {
-          best = v[i];
-          bid = e;
-        }
+      // ascending e within the lane: ties keep the lower id
+      if (e < E && !((taken >> i) & 1u) && (bid == 0x7fffffff || v[i] > best)) {
+        best = v[i];
+        bid = e;
       }
     }
 #pragma unroll
@@ -128,28 +126,32 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict
       }
     }
     if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-    sel_v[s] = best;
-    sel_id[s] = bid;
+    if (lane == s) {
+      my_v = best;
+      my_id = bid;
+    }
   }
-  if (lane == 0) {
-    const float m = sel_v[0];
-    float e[16];
-    float sum = 0.f;
-    for (int s = 0; s < k; ++s) {
-      e[s] = expf(sel_v[s] - m);
-      sum = sum + e[s];
-    }
-    for (int s = 0; s < k; ++s) {
-      ids[static_cast<int64_t>(warp) * k + s] = sel_id[s];
-      w[static_cast<int64_t>(warp) * k + s] = __fdiv_rn(e[s], sum);
-    }
+  // softmax over the k selected logits, max (selection 0) subtracted, summed in slot order
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = lane < k ? expf(my_v - m) : 0.f;
+  float sum = 0.f;
+  for (int s = 0; s < k; ++s) sum = sum + __shfl_sync(0xffffffffu, ex, s);
+  if (lane < k) {
+    ids[static_cast<int64_t>(warp) * k + lane] = my_id;
+    w[static_cast<int64_t>(warp) * k + lane] = __fdiv_rn(ex, sum);
   }
 }
 
 moex_status launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s) {
   const int threads = 128;
   const int grid = (T * 32 + threads - 1) / threads;
-  return cuda_status(launch_pdl(route_topk_kernel, dim3(grid), dim3(threads), 0, s, logits, T, E, k, ids, w));
+  if (E <= 128)
+    return cuda_status(launch_pdl(route_topk_kernel<4>, dim3(grid), dim3(threads), 0, s, logits, T, E, k, ids, w));
+  if (E <= 256)
+    return cuda_status(launch_pdl(route_topk_kernel<8>, dim3(grid), dim3(threads), 0, s, logits, T, E, k, ids, w));
+  if (E <= 512)
+    return cuda_status(launch_pdl(route_topk_kernel<16>, dim3(grid), dim3(threads), 0, s, logits, T, E, k, ids, w));
+  return cuda_status(launch_pdl(route_topk_kernel<32>, dim3(grid), dim3(threads), 0, s, logits, T, E, k, ids, w));
 }
 
 }  // namespace moex
