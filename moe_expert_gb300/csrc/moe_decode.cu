@@ -313,25 +313,6 @@ __global__ void __launch_bounds__(MAXT, 1) moe_gu_kernel(DecodeArgs a) {
   for (int j = threadIdx.x; j < a.n; j += blockDim.x) ids_s[j] = a.ids[j];
   __syncthreads();
   build_groups(G, ids_s, a.n, a.E, a.status, ids_s + MAX_ENTRIES);
-  // q8_1 of the layer input (same block arithmetic as quantize_q8_1)
-  for (int t = threadIdx.x; t < a.T * NB; t += blockDim.x) {
-    const int tok = t / NB, b = t % NB;
-    float v[QK];
-    const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<int64_t>(tok) * a.H + b * QK);
-#pragma unroll
-    for (int i = 0; i < QK / 4; ++i) {
-      const float4 f = src[i];
-      v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
-    }
-    uint32_t qw[8];
-    float d, s_;
-    q8_1_block(v, qw, &d, &s_);
-    uint4* dst = reinterpret_cast<uint4*>(xs + tok * a.H + b * QK);
-    dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-    dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-    xd[tok * NB + b] = d;
-  }
-  __syncthreads();
   MOEX_TRACE_STAMP(2);
   pdl_launch_dependents();  // after the wait: the routing ids are complete
 
@@ -340,6 +321,7 @@ __global__ void __launch_bounds__(MAXT, 1) moe_gu_kernel(DecodeArgs a) {
   const int nunit = units > static_cast<int>(blockIdx.x) ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
 
   if (warp == nwc) {
+    // the weight stream starts as soon as the groups are known
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
       int issued = 0;
@@ -364,6 +346,27 @@ __global__ void __launch_bounds__(MAXT, 1) moe_gu_kernel(DecodeArgs a) {
     }
     return;
   }
+
+  // consumers: q8_1 of the layer input (same block arithmetic as quantize_q8_1)
+  const int nthr = nwc * 32;
+  for (int t = threadIdx.x; t < a.T * NB; t += nthr) {
+    const int tok = t / NB, b = t % NB;
+    float v[QK];
+    const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<int64_t>(tok) * a.H + b * QK);
+#pragma unroll
+    for (int i = 0; i < QK / 4; ++i) {
+      const float4 f = src[i];
+      v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+    }
+    uint32_t qw[8];
+    float d, s_;
+    q8_1_block(v, qw, &d, &s_);
+    uint4* dst = reinterpret_cast<uint4*>(xs + tok * a.H + b * QK);
+    dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+    dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+    xd[tok * NB + b] = d;
+  }
+  named_bar_sync(1, nthr);
 
   const ConsumerPos pos = consumer_pos(warp, lane, WPS);
   bool dead = false;
