@@ -643,7 +643,7 @@ template <int FMT>
 moex_status launch_dn_fmt(const DecodeArgs& a, int cap, cudaStream_t s) {
   const int NS = num_slices(a.I / QK);
   const int wps = decode_wps(NS);
-  if (wps == 4) return launch_dn<FMT, 4, 416>(a, cap, s);
+  if (wps == 4) return launch_dn<FMT, 5, 512>(a, cap, s);  // five teams of up to three slice warps
   if (wps == 2) return (NS * 2 + 1) * 32 <= 352 ? launch_dn<FMT, 2, 352>(a, cap, s) : launch_dn<FMT, 2, 544>(a, cap, s);
   return (NS + 1) * 32 <= 352 ? launch_dn<FMT, 1, 352>(a, cap, s) : launch_dn<FMT, 1, 544>(a, cap, s);
 }
