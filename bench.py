@@ -560,7 +560,8 @@ def run_reference(args, ws, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64+f64",
             "data": "synthetic",
             "config": {"workload": "Q8_0 decode GEMV 8192x2560 x q8_1 activations, ncols 1/2/4/8 per step "
-                                   "(quantize_q8_1 + qgemv each), cold weights",
+                                   "(one quantize_q8_1 of the step's 15 columns, then a qgemv per column count), "
+                                   "cold weights",
                        "rows": ROWS, "K": K, "ncols": list(NCOLS), "parallelism": "cpu"},
             "gpu_launches": 0,
             "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": max(1, round(cpu / wall)),
