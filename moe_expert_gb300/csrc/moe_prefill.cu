@@ -192,8 +192,8 @@ __global__ void __launch_bounds__(1024) prefill_scan_kernel(int n, int E, int* _
 }
 
 // Both tile lists, one thread per tile: token tile g belongs to the last
-// expert e with etb[e] <= g; its ceil(n_e / 192) token tiles split the
-// expert's rows evenly.
+// expert e with etb[e] <= g; its ceil(n_e / 192) token tiles take 192 rows
+// each, the last one the rest.
 __global__ void __launch_bounds__(256) prefill_tiles_kernel(int E, const int* __restrict__ counts,
                                                             const int* __restrict__ eoff, const int* __restrict__ etb,
                                                             PrefillTiles tl) {
@@ -213,9 +213,11 @@ __global__ void __launch_bounds__(256) prefill_tiles_kernel(int E, const int* __
   }
   const int e = lo;
   const int64_t ne = counts[e];
-  const int64_t ntt = pf_token_tiles(static_cast<int>(ne));
   const int64_t tt = g - etb[e];
-  const int r0 = eoff[e] + static_cast<int>(tt * ne / ntt), r1 = eoff[e] + static_cast<int>((tt + 1) * ne / ntt);
+  // full tiles of PF_NMAX rows and one ragged last tile: every token box but
+  // the last of an expert is full, so no loaded row is padding
+  const int r0 = eoff[e] + static_cast<int>(tt * PF_NMAX);
+  const int r1 = eoff[e] + static_cast<int>((tt + 1) * PF_NMAX < ne ? (tt + 1) * PF_NMAX : ne);
   (first ? tl.t1 : tl.t2)[j] = make_int4(e, f, r0, r1 - r0);
 }
 
