@@ -10,38 +10,51 @@ namespace moex {
 
 // ----------------------------------------------------------------- q8_1
 
-// One thread per 32-value block (#1525 Change: quantize_mmq_q8_1; the block
-// arithmetic is q8_1_block, shared with every fused quantiser).
+// Eight lanes per 32-value block, four values a lane (#1525 Change:
+// quantize_mmq_q8_1).  Same arithmetic as q8_1_block: amax over the block
+// (shuffles), d = amax / 127 and every q = roundf(x / d) by IEEE division,
+// s = d * (sum of q), an all-zero block giving zeros; each lane stores its
+// four quants as one word, so a block's 32 bytes go out in one store.
 __global__ void __launch_bounds__(128) quantize_q8_1_kernel(const float* __restrict__ x, int K, int NB, int ncols,
                                                             int64_t ldx, int8_t* __restrict__ q,
                                                             float* __restrict__ ds) {
   pdl_wait();
   pdl_launch_dependents();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= ncols * NB) return;
-  const int c = t / NB, b = t % NB;
-  const float4* src = reinterpret_cast<const float4*>(x + c * ldx + static_cast<int64_t>(b) * QK);
-  float v[QK];
+  const int blk = t >> 3, sub = t & 7;   // block index, lane within the block's group of 8
+  const bool valid = blk < ncols * NB;
+  const int c = valid ? blk / NB : 0, b = valid ? blk % NB : 0;
+  float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (valid) f = reinterpret_cast<const float4*>(x + c * ldx + static_cast<int64_t>(b) * QK)[sub];
+  float amax = fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w)));
 #pragma unroll
-  for (int i = 0; i < QK / 4; ++i) {
-    const float4 f = src[i];
-    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+  for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float d = __fdiv_rn(amax, 127.0f);
+  const float v[4] = {f.x, f.y, f.z, f.w};
+  int sum = 0;
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    int qi = 0;
+    if (amax > 0.f) qi = static_cast<int>(roundf(__fdiv_rn(v[i], d)));
+    sum += qi;
+    packed |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * i);
   }
-  uint32_t qw[8];
-  float d, s;
-  q8_1_block(v, qw, &d, &s);
-  uint4* dst = reinterpret_cast<uint4*>(q + static_cast<int64_t>(c) * K + static_cast<int64_t>(b) * QK);
-  dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-  dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-  reinterpret_cast<float2*>(ds)[static_cast<int64_t>(c) * NB + b] = make_float2(d, s);
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (!valid) return;
+  reinterpret_cast<uint32_t*>(q + static_cast<int64_t>(c) * K + static_cast<int64_t>(b) * QK)[sub] = packed;
+  if (sub == 0)
+    reinterpret_cast<float2*>(ds)[static_cast<int64_t>(c) * NB + b] =
+        amax > 0.f ? make_float2(d, __fmul_rn(d, static_cast<float>(sum))) : make_float2(0.f, 0.f);
 }
 
 moex_status launch_quantize_q8_1(const float* x, int64_t K, int ncols, int64_t ldx, int8_t* q, float* ds,
                                  cudaStream_t s) {
   const int NB = static_cast<int>(K / QK);
-  const int n = ncols * NB;
-  return cuda_status(launch_pdl(quantize_q8_1_kernel, dim3((n + 127) / 128), dim3(128), 0, s, x,
-                                static_cast<int>(K), NB, ncols, ldx, q, ds));
+  const int64_t threads = static_cast<int64_t>(ncols) * NB * 8;
+  return cuda_status(launch_pdl(quantize_q8_1_kernel, dim3(static_cast<unsigned>((threads + 127) / 128)), dim3(128),
+                                0, s, x, static_cast<int>(K), NB, ncols, ldx, q, ds));
 }
 
 // ----------------------------------------------------------------- weight pack
