@@ -14,12 +14,11 @@
 //    its 16 lanes x 2 halves hold one 32-value block each, with the
 //    activations of that block for all columns in registers (loaded once per
 //    column set), so activations cost no shared-memory traffic per row;
-//  * every lane streams exactly the weight bytes it will consume (its block
-//    of each of its rows) with 16-byte cp.async copies into its own slots of
-//    a shared-memory ring, several 8-row stages ahead: tens of KB per SM stay
-//    in flight without holding registers, a warp's copies cover contiguous
-//    512-byte row pieces, and no producer warp, mbarrier or cross-warp
-//    handshake is needed for the weights;
+//  * weights arrive in stages of 8 consecutive rows: either through a
+//    shared-memory ring that one producer thread fills with two bulk (TMA)
+//    copies a stage (the 8 rows' quants, then their scales), or, in the
+//    register-staged GEMV, as each lane's own 16-byte loads of its block of
+//    each row;
 //  * a stage of 8 rows is shared by all warps (every slice, every row), so
 //    the last stage to arrive is finished quickly;
 //  * per-lane partial sums are reduced over the 16 lanes with a recursive
@@ -37,7 +36,6 @@ namespace moex {
 
 constexpr int SR = 8;        // rows per pipeline stage
 constexpr int SLICE = 16;    // blocks per K slice (one per lane of a half warp)
-constexpr int NRED = 4;      // slots of the cross-slice reduction buffer
 
 __host__ __device__ inline int64_t qs_row_bytes(int fmt, int64_t K) { return fmt == MOEX_Q8_0 ? K : K / 2; }
 __host__ __device__ inline int64_t sc_row_bytes(int64_t K) { return ((K / QK) * 2 + 15) / 16 * 16; }
@@ -170,7 +168,7 @@ __device__ __forceinline__ void halving_reduce(float* v, int lane) {
 
 __host__ __device__ constexpr int pow2_ceil(int v) { return v <= 1 ? 1 : 2 * pow2_ceil((v + 1) / 2); }
 
-// ----------------------------------------------------------------- lane ring
+// ----------------------------------------------------------------- consumer layout
 
 // Warp w owns slice ks = w / WPS; its half `hf` (lane >> 4) and index
 // jw = w % WPS give the stage rows jw*2 + hf + 2*WPS*i, i < RPH, with
@@ -190,118 +188,6 @@ __device__ __forceinline__ ConsumerPos consumer_pos(int warp, int lane, int WPS)
   return p;
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Waits until at most n of this thread's most recent cp.async groups are pending.
-__device__ __forceinline__ void cp_async_wait(int n) {
-  switch (n) {
-    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
-    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
-    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
-    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
-    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
-    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
-    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
-    case 7: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
-    default: asm volatile("cp.async.wait_group 8;" ::: "memory"); break;
-  }
-}
-
-// Geometry of the per-lane ring.  One ring slot holds one 8-row stage:
-//   quants: [rr][chunk][warp][lane] x 16 bytes  (a warp's accesses for one
-//           (rr, chunk) are 512 contiguous bytes: no bank conflicts)
-//   scales: [rr][warp][lane] x 4 bytes (the FP16 scale word holding the
-//           lane's block; block b is its half b & 1)
-template <int FMT, int WPS>
-struct Ring {
-  static constexpr int RPH = SR / (2 * WPS);
-  static constexpr int QB = FmtTraits<FMT>::QBYTES;
-  static constexpr int NCH = QB / 16;
-  __host__ __device__ static int slot_bytes(int nwc) { return nwc * 32 * RPH * (NCH * 16 + 4); }
-  __device__ static uint8_t* qptr(uint8_t* slot, int nwc, int rr, int h, int warp, int lane) {
-    return slot + ((((rr * NCH + h) * nwc + warp) * 32 + lane) * 16);
-  }
-  __device__ static uint8_t* sptr(uint8_t* slot, int nwc, int rr, int warp, int lane) {
-    return slot + nwc * 32 * RPH * NCH * 16 + (((rr * nwc + warp) * 32 + lane) * 4);
-  }
-};
-
-// Issues this lane's copies of one stage into `slot`: rows [0, nrows) of the
-// stage start at qsrc / ssrc (plane row strides qrow / scrow).  The caller
-// commits the group.
-template <int FMT, int WPS>
-__device__ __forceinline__ void ring_issue(uint8_t* slot, int nwc, const ConsumerPos& p, const uint8_t* qsrc,
-                                           const uint8_t* ssrc, int nrows, int qrow, int scrow, int NB) {
-  using R = Ring<FMT, WPS>;
-  const int b = p.ks * SLICE + p.li;
-  if (b >= NB) return;
-#pragma unroll
-  for (int rr = 0; rr < R::RPH; ++rr) {
-    const int row = p.jw * 2 + p.hf + 2 * WPS * rr;
-    if (row < nrows) {
-      const uint8_t* q = qsrc + static_cast<int64_t>(row) * qrow + b * R::QB;
-#pragma unroll
-      for (int h = 0; h < R::NCH; ++h) cp_async16(R::qptr(slot, nwc, rr, h, p.warp, p.lane), q + 16 * h);
-      cp_async4(R::sptr(slot, nwc, rr, p.warp, p.lane), ssrc + static_cast<int64_t>(row) * scrow + 4 * (b >> 1));
-    }
-  }
-}
-
-// Asks L2 for the 128-byte lines of this lane's part of one stage (one lane
-// in four: a line holds the pieces of four neighbouring lanes).
-template <int FMT, int WPS>
-__device__ __forceinline__ void lane_prefetch_l2(const ConsumerPos& p, const uint8_t* qsrc, const uint8_t* ssrc,
-                                                 int nrows, int qrow, int scrow, int NB) {
-  using R = Ring<FMT, WPS>;
-  const int b = p.ks * SLICE + p.li;
-  if (b >= NB || (p.li & 3) != 0) return;
-#pragma unroll
-  for (int rr = 0; rr < R::RPH; ++rr) {
-    const int row = p.jw * 2 + p.hf + 2 * WPS * rr;
-    if (row < nrows) {
-      const uint8_t* q = qsrc + static_cast<int64_t>(row) * qrow + b * R::QB;
-#pragma unroll
-      for (int h = 0; h < R::NCH * 4; h += 8)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(q + 16 * h) : "memory");
-      if ((p.li & 15) == 0)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(ssrc + static_cast<int64_t>(row) * scrow + 4 * (b >> 1))
-                     : "memory");
-    }
-  }
-}
-
-// Per-lane partial sums of one stage from the ring: v[rr*C + c] for this
-// lane's rows (zero for rows >= nrows or blocks >= NB).
-template <int FMT, int C, int WPS, int N>
-__device__ __forceinline__ void ring_partials(uint8_t* slot, int nwc, const ConsumerPos& p, int nrows, int NB,
-                                              const ActRegs<FMT, C>& act, float (&v)[N]) {
-  using R = Ring<FMT, WPS>;
-#pragma unroll
-  for (int i = 0; i < N; ++i) v[i] = 0.f;
-  const int b = p.ks * SLICE + p.li;
-  if (b >= NB) return;
-#pragma unroll
-  for (int rr = 0; rr < R::RPH; ++rr) {
-    const int row = p.jw * 2 + p.hf + 2 * WPS * rr;
-    if (row < nrows) {
-      const uint4 q0 = *reinterpret_cast<const uint4*>(R::qptr(slot, nwc, rr, 0, p.warp, p.lane));
-      const uint4 q1 = R::NCH > 1 ? *reinterpret_cast<const uint4*>(R::qptr(slot, nwc, rr, R::NCH - 1, p.warp, p.lane))
-                                  : q0;
-      const uint32_t sw = *reinterpret_cast<const uint32_t*>(R::sptr(slot, nwc, rr, p.warp, p.lane));
-      const uint16_t hb = static_cast<uint16_t>((b & 1) ? (sw >> 16) : (sw & 0xFFFFu));
-      const float dw = __half2float(__ushort_as_half(hb));
-      block_dots_from<FMT, C>(q0, q1, dw, act, &v[rr * C]);
-    }
-  }
-}
-
-// Reduces a lane's partials over its half warp and hands each (row, c) sum
-// of this slice to out(row, c, value) (row < nrows).
 template <int C, int WPS, int N, typename Out>
 __device__ __forceinline__ void reduce_out(float (&v)[N], const ConsumerPos& p, int nrows, Out&& out) {
   constexpr int RPH = SR / (2 * WPS);
@@ -356,50 +242,8 @@ __device__ __forceinline__ bool red_slot_wait(volatile int* seq, int it, volatil
   }
 }
 
-// Final sum over slices (in slice order) of red[row][ks][c] for one stage,
-// run by one warp.  Calls out(row, c, value) for row < nrows, c < C.
-template <int C, typename Out>
-__device__ __forceinline__ void stage_final(const float* red, int nrows, int NS, int lane, Out&& out) {
-  for (int idx = lane; idx < nrows * C; idx += 32) {
-    const int row = idx / C, c = idx % C;
-    float s = red[(row * NS + 0) * C + c];
-    for (int ks = 1; ks < NS; ++ks) s = s + red[(row * NS + ks) * C + c];
-    out(row, c, s);
-  }
-}
-
-// Marks one consumer warp done with a stage; returns true for the last warp
-// (which then owns the final sum).  Shared-memory counter per slot.
-__device__ __forceinline__ bool stage_arrive_last(int* cnt, int nwarps, int lane) {
-  int old = 0;
-  __syncwarp();
-  if (lane == 0) {
-    __threadfence_block();
-    old = atomicAdd(cnt, 1);
-  }
-  old = __shfl_sync(0xffffffffu, old, 0);
-  const bool last = old == nwarps - 1;
-  if (last) __threadfence_block();
-  return last;
-}
-
-// Consumer warp count for a K with NB blocks, and warps per slice.
+// K slices (of 16 blocks) of a row with NB blocks.
 __host__ __device__ inline int num_slices(int NB) { return (NB + SLICE - 1) / SLICE; }
-__host__ __device__ inline int warps_per_slice(int NS) { return NS <= 3 ? 4 : (NS <= 7 ? 2 : 1); }
-
-// ----------------------------------------------------------------- L2 prefetch
-
-// Asks the TMA unit to bring [src, src+bytes) into L2 (no shared memory, no
-// completion); src and bytes multiples of 16.  Issued in pieces of <= 64 KB.
-__device__ __forceinline__ void prefetch_l2(const void* src, int64_t bytes) {
-  const uint8_t* p = static_cast<const uint8_t*>(src);
-  while (bytes > 0) {
-    const uint32_t n = static_cast<uint32_t>(bytes < 65536 ? bytes : 65536);
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
-    p += n;
-    bytes -= n;
-  }
-}
 
 // ----------------------------------------------------------------- TMA ring
 
