@@ -212,8 +212,8 @@ moex_status moex_moe_prefill_workspace_layout(int T, int k, int E, int64_t hidde
  *            moex_route_topk); out : device FP32 [T][hidden] (overwritten).
  *   ws     : device workspace of moex_moe_prefill_workspace_bytes() bytes.
  * hidden % 128 == 0, inter % 64 == 0, E <= 4096, E * 2 * inter < 2^31.
- * Eight launches (sort: histogram, scan, tiles, scatter; gather; GEMM 1;
- * clear; GEMM 2); the GEMMs use tcgen05 / TMEM / TMA.  An entry whose id is
+ * Seven launches (sort: histogram, scan, tiles, scatter; gather, which also
+ * clears out; GEMM 1; GEMM 2); the GEMMs use tcgen05 / TMEM / TMA.  An entry whose id is
  * outside [0, E) is left out of the layer and flagged (MOEX_EDEVICE).
  */
 moex_status moex_moe_prefill(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16, int T,
