@@ -343,19 +343,21 @@ moex_status launch_reg(const GemvArgs& a, cudaStream_t s) {
 // larger K one warp per slice and one CTA per SM.
 template <int FMT, int C>
 moex_status launch_c(const GemvArgs& a, int smem_cap, cudaStream_t s) {
-  if constexpr (C <= (FMT == MOEX_IQ4_NL ? 4 : 2)) {
-    // stages ahead and CTAs per SM: the pipelined half-SM form where the
-    // registers allow it, else every stage in flight at once
+  if constexpr (C <= 4) {
+    // register-staged, P stages ahead: one column streams 3 (IQ4_NL 4)
+    // stages ahead at two CTAs per SM; two columns keep every stage in
+    // flight; three and four columns stream 4 (IQ4_NL 6) ahead, one CTA per SM
     constexpr int NSTG = FMT == MOEX_IQ4_NL ? 12 : 8;
     constexpr bool HALF = C == 1;
-    constexpr int P = !HALF ? NSTG : FMT == MOEX_Q8_0 ? 3 : 4;
+    constexpr int P = HALF ? (FMT == MOEX_Q8_0 ? 3 : 4) : C <= 2 ? NSTG : (FMT == MOEX_Q8_0 ? 4 : 6);
     if (a.NS <= 5 && a.rows <= static_cast<int64_t>(sm_count()) * SR * NSTG * 4)
       return launch_reg<FMT, C, NSTG, P, HALF ? 2 : 1>(a, s);
   }
   if (a.NS <= 5) {
-    // up to 4 columns: two warps per slice, two CTAs per SM (the next GEMV
-    // overlaps this one's drain); more columns are compute-bound: one CTA
-    // per SM with twice the warps, the columns split over two warp groups
+    // (K beyond the register-staged limits) up to 4 columns: two warps per
+    // slice, two CTAs per SM (the next GEMV overlaps this one's drain); more
+    // columns are compute-bound: one CTA per SM with twice the warps, the
+    // columns split over two warp groups
     if constexpr (C <= 4) return launch_one<FMT, C, 2, 2>(a, smem_cap, s);
     else if constexpr (C % 2 == 0) return launch_one<FMT, C, 2, 1, 2>(a, smem_cap, s);
     else return launch_one<FMT, C, 2, 1>(a, smem_cap, s);

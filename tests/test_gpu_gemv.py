@@ -104,3 +104,18 @@ def test_config_q8_0_8192x2560(ncols):
 def test_config_iq4_nl_12288x2560(ncols):
     _, _, _, y, ref, A, _, _ = _run("iq4_nl", 12288, 2560, ncols, seed=0)
     assert_within(y, ref, A, f"iq4_nl 12288x2560 c{ncols}")
+
+
+@pytest.mark.parametrize("fmt,ncols", [("q8_0", 3), ("iq4_nl", 11)])
+def test_strided_output_leaves_padding(fmt, ncols):
+    """y with a leading dimension above rows: column c at y + c*ldy; the
+    padding between columns is never written."""
+    import torch
+    import moe_expert_gb300 as mx
+    rows, K, pad = 300, 1024, 37
+    W, xq, xds, y, ref, A, _, _ = _run(fmt, rows, K, ncols, seed=21)
+    big = torch.full((ncols, rows + pad), float("nan"), dtype=torch.float32, device="cuda")
+    mx.qgemv(W, xq, xds, big[:, :rows])
+    got = to_np(big)
+    assert np.array_equal(got[:, :rows].view(np.uint32), y.view(np.uint32))
+    assert np.all(np.isnan(got[:, rows:]))
