@@ -452,6 +452,12 @@ def run_ours(args, ws, rank, local):
         detail["iq4_nl_12288x2560"] = gemv_detail(iq, (1, 2, 3, 4, 8), 2000, peak)
         del iq
         torch.cuda.empty_cache()
+        head = GemvCase("q8_0", 128256, K, (1, 8), l2)
+        for c in (1, 8):
+            mx.quantize_q8_1(head.x[c], head.xq[c], head.xds[c])
+        detail["q8_0_head_128256x2560"] = gemv_detail(head, (1, 8), 200, peak)
+        del head
+        torch.cuda.empty_cache()
         small = GemvCase("q8_0", 512, 2048, (1,), l2)
         mx.quantize_q8_1(small.x[1], small.xq[1], small.xds[1])
         detail["q8_0_512x2048"] = gemv_detail(small, (1,), 2000, peak)

@@ -171,6 +171,17 @@ moex_status moex_moe_decode(const moex_qweight* gate_up, const moex_qweight* dow
                             moex_stream stream);
 
 /*
+ * moex_moe_decode with the residual add fused into the combine (#1525
+ * Change: the MoE combine folded into the write of the layer output, no
+ * round trip of the combined rows): out[t] = residual[t] + (the combine of
+ * moex_moe_decode, summed in slot order first), one FP32 addition.
+ *   residual : device FP32 [T][hidden], 16-byte aligned; may be out itself.
+ */
+moex_status moex_moe_decode_residual(const moex_qweight* gate_up, const moex_qweight* down, const float* x, int T,
+                                     const int32_t* ids, const float* w, int k, const float* residual, float* out,
+                                     void* ws, size_t ws_bytes, moex_stream stream);
+
+/*
  * moex_moe_decode that also writes its intermediates, for staged checking:
  *   gu_dbg : device FP32 [T*k][2*inter] gate/up outputs (may be NULL)
  *   h_dbg  : device FP32 [T*k][inter] H before its q8_1 (may be NULL)
@@ -219,6 +230,16 @@ moex_status moex_moe_prefill_workspace_layout(int T, int k, int E, int64_t hidde
 moex_status moex_moe_prefill(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16, int T,
                              const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,
                              moex_stream stream);
+
+/*
+ * moex_moe_prefill with the residual add fused (#1525 Change): out starts as
+ * residual instead of zero, and the second GEMM adds every weighted expert
+ * output to it (the order of those FP32 additions is not fixed).
+ *   residual : device FP32 [T][hidden], 16-byte aligned; may be out itself.
+ */
+moex_status moex_moe_prefill_residual(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16,
+                                      int T, const int32_t* ids, const float* w, int k, const float* residual,
+                                      float* out, void* ws, size_t ws_bytes, moex_stream stream);
 
 /*
  * moex_moe_decode without a workspace argument, for callers that cannot

@@ -64,6 +64,10 @@ SIGNATURES = {
                                                          ctypes.POINTER(_SZ)]),
     "moex_moe_prefill": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _SZ, _P]),
     "moex_moe_decode_noalloc": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P]),
+    "moex_moe_decode_residual": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _P, _SZ,
+                                                _P]),
+    "moex_moe_prefill_residual": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _P, _SZ,
+                                                 _P]),
 }
 
 _lib = None
@@ -228,11 +232,13 @@ def moe_decode_workspace_bytes(T: int, k: int, hidden: int, inter: int) -> int:
 
 
 def moe_decode(gate_up: PackedWeight, down: PackedWeight, x, ids, w, out=None, ws=None, debug=False,
-               stream=None):
+               stream=None, residual=None):
     """The grouped MoE decode layer.  x [T, hidden] FP32, ids/w [T, k].
 
     Returns out [T, hidden]; with debug=True returns (out, dict of the
-    intermediates gu [T*k, 2I], h [T*k, I], hq [T*k, I], hds [T*k, I/32, 2])."""
+    intermediates gu [T*k, 2I], h [T*k, I], hq [T*k, I], hds [T*k, I/32, 2]).
+    With residual [T, hidden] FP32 (may be out) the layer writes
+    residual + combine (moex_moe_decode_residual)."""
     torch = _torch()
     T, hidden = x.shape
     k = ids.shape[1]
@@ -243,6 +249,13 @@ def moe_decode(gate_up: PackedWeight, down: PackedWeight, x, ids, w, out=None, w
     if ws is None:
         ws = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
     st = _stream(stream)
+    if residual is not None:
+        if debug:
+            raise ValueError("residual and debug are separate entry points")
+        _check(lib().moex_moe_decode_residual(ctypes.byref(gate_up.struct), ctypes.byref(down.struct), _ptr(x), T,
+                                              _ptr(ids), _ptr(w), k, _ptr(residual), _ptr(out), _ptr(ws),
+                                              ws.numel(), st), "moex_moe_decode_residual")
+        return out
     if not debug:
         _check(lib().moex_moe_decode(ctypes.byref(gate_up.struct), ctypes.byref(down.struct), _ptr(x), T,
                                      _ptr(ids), _ptr(w), k, _ptr(out), _ptr(ws), ws.numel(), st),
@@ -271,9 +284,12 @@ def moe_prefill_workspace_layout(T: int, k: int, E: int, hidden: int, inter: int
     return [int(v) for v in off]
 
 
-def moe_prefill(gate_up: PackedWeight, down: PackedWeight, x_bf16, ids, w, out=None, ws=None, stream=None):
+def moe_prefill(gate_up: PackedWeight, down: PackedWeight, x_bf16, ids, w, out=None, ws=None, stream=None,
+                residual=None):
     """The grouped MoE prefill layer.  x_bf16: BF16 (or raw uint16/int16 bit
-    patterns) [T, hidden]; ids / w [T, k].  Returns out [T, hidden] FP32."""
+    patterns) [T, hidden]; ids / w [T, k].  Returns out [T, hidden] FP32;
+    with residual [T, hidden] FP32 (may be out), residual + the layer
+    (moex_moe_prefill_residual)."""
     torch = _torch()
     T, hidden = x_bf16.shape
     k = ids.shape[1]
@@ -283,6 +299,11 @@ def moe_prefill(gate_up: PackedWeight, down: PackedWeight, x_bf16, ids, w, out=N
     if ws is None:
         ws = torch.empty(moe_prefill_workspace_bytes(T, k, E, hidden, inter), dtype=torch.uint8,
                          device=x_bf16.device)
+    if residual is not None:
+        _check(lib().moex_moe_prefill_residual(ctypes.byref(gate_up.struct), ctypes.byref(down.struct), _ptr(x_bf16),
+                                               T, _ptr(ids), _ptr(w), k, _ptr(residual), _ptr(out), _ptr(ws),
+                                               ws.numel(), _stream(stream)), "moex_moe_prefill_residual")
+        return out
     _check(lib().moex_moe_prefill(ctypes.byref(gate_up.struct), ctypes.byref(down.struct), _ptr(x_bf16), T,
                                   _ptr(ids), _ptr(w), k, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
            "moex_moe_prefill")

@@ -95,6 +95,27 @@ moex_status check_weight(const moex_qweight* w) {
   return MOEX_OK;
 }
 
+moex_status prefill_checked(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16, int T,
+                            const int32_t* ids, const float* w, int k, const float* residual, float* out, void* ws,
+                            size_t ws_bytes, moex_stream stream) {
+  moex_status st = check_weight(gate_up);
+  if (st != MOEX_OK) return st;
+  st = check_weight(down);
+  if (st != MOEX_OK) return st;
+  if (gate_up->fmt != MOEX_IQ4_NL || down->fmt != MOEX_IQ4_NL) return MOEX_EUNSUPPORTED;
+  if (!x_bf16 || !ids || !w || !out || !ws) return MOEX_EINVAL;
+  if (T < 1 || k < 1 || k > 16 || static_cast<int64_t>(T) * k > (int64_t(1) << 26)) return MOEX_EINVAL;
+  if (gate_up->n_mats != down->n_mats || gate_up->n_mats > 4096) return MOEX_EINVAL;
+  if (gate_up->rows % 2 != 0 || down->rows != gate_up->K || down->K != gate_up->rows / 2) return MOEX_EINVAL;
+  if (gate_up->K % 128 != 0 || down->K % 64 != 0) return MOEX_EUNSUPPORTED;
+  // weight rows are 32-bit tensor-map coordinates
+  if (static_cast<int64_t>(gate_up->n_mats) * gate_up->rows > INT32_MAX) return MOEX_EUNSUPPORTED;
+  if (ws_bytes < moe_prefill_ws_bytes(T, k, gate_up->n_mats, gate_up->K, down->K)) return MOEX_ENOSPACE;
+  if (!aligned16(x_bf16) || !aligned16(ws) || !aligned16(out)) return MOEX_EALIGN;
+  if (residual && !aligned16(residual)) return MOEX_EALIGN;
+  return launch_moe_prefill(gate_up, down, x_bf16, T, ids, w, k, residual, out, ws, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -193,7 +214,18 @@ moex_status moex_moe_decode(const moex_qweight* gate_up, const moex_qweight* dow
   const moex_status st = check_decode(gate_up, down, x, T, ids, w, k, out, ws, ws_bytes);
   if (st != MOEX_OK) return st;
   return launch_moe_decode(gate_up, down, x, T, ids, w, k, out, ws, ws_bytes, nullptr, nullptr, nullptr, nullptr,
-                           stream);
+                           nullptr, stream);
+}
+
+moex_status moex_moe_decode_residual(const moex_qweight* gate_up, const moex_qweight* down, const float* x, int T,
+                                     const int32_t* ids, const float* w, int k, const float* residual, float* out,
+                                     void* ws, size_t ws_bytes, moex_stream stream) {
+  const moex_status st = check_decode(gate_up, down, x, T, ids, w, k, out, ws, ws_bytes);
+  if (st != MOEX_OK) return st;
+  if (!residual) return MOEX_EINVAL;
+  if (!aligned16(residual)) return MOEX_EALIGN;
+  return launch_moe_decode(gate_up, down, x, T, ids, w, k, out, ws, ws_bytes, nullptr, nullptr, nullptr, nullptr,
+                           residual, stream);
 }
 
 moex_status moex_moe_decode_debug(const moex_qweight* gate_up, const moex_qweight* down, const float* x, int T,
@@ -203,7 +235,7 @@ moex_status moex_moe_decode_debug(const moex_qweight* gate_up, const moex_qweigh
   const moex_status st = check_decode(gate_up, down, x, T, ids, w, k, out, ws, ws_bytes);
   if (st != MOEX_OK) return st;
   return launch_moe_decode(gate_up, down, x, T, ids, w, k, out, ws, ws_bytes, gu_dbg, h_dbg, hq_dbg, hds_dbg,
-                           stream);
+                           nullptr, stream);
 }
 
 size_t moex_moe_prefill_workspace_bytes(int T, int k, int E, int64_t hidden, int64_t inter) {
@@ -218,24 +250,18 @@ moex_status moex_moe_prefill_workspace_layout(int T, int k, int E, int64_t hidde
   return MOEX_OK;
 }
 
+
 moex_status moex_moe_prefill(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16, int T,
                              const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,
                              moex_stream stream) {
-  moex_status st = check_weight(gate_up);
-  if (st != MOEX_OK) return st;
-  st = check_weight(down);
-  if (st != MOEX_OK) return st;
-  if (gate_up->fmt != MOEX_IQ4_NL || down->fmt != MOEX_IQ4_NL) return MOEX_EUNSUPPORTED;
-  if (!x_bf16 || !ids || !w || !out || !ws) return MOEX_EINVAL;
-  if (T < 1 || k < 1 || k > 16 || static_cast<int64_t>(T) * k > (int64_t(1) << 26)) return MOEX_EINVAL;
-  if (gate_up->n_mats != down->n_mats || gate_up->n_mats > 4096) return MOEX_EINVAL;
-  if (gate_up->rows % 2 != 0 || down->rows != gate_up->K || down->K != gate_up->rows / 2) return MOEX_EINVAL;
-  if (gate_up->K % 128 != 0 || down->K % 64 != 0) return MOEX_EUNSUPPORTED;
-  // weight rows are 32-bit tensor-map coordinates
-  if (static_cast<int64_t>(gate_up->n_mats) * gate_up->rows > INT32_MAX) return MOEX_EUNSUPPORTED;
-  if (ws_bytes < moe_prefill_ws_bytes(T, k, gate_up->n_mats, gate_up->K, down->K)) return MOEX_ENOSPACE;
-  if (!aligned16(x_bf16) || !aligned16(ws) || !aligned16(out)) return MOEX_EALIGN;
-  return launch_moe_prefill(gate_up, down, x_bf16, T, ids, w, k, out, ws, stream);
+  return prefill_checked(gate_up, down, x_bf16, T, ids, w, k, nullptr, out, ws, ws_bytes, stream);
+}
+
+moex_status moex_moe_prefill_residual(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16,
+                                      int T, const int32_t* ids, const float* w, int k, const float* residual,
+                                      float* out, void* ws, size_t ws_bytes, moex_stream stream) {
+  if (!residual) return MOEX_EINVAL;
+  return prefill_checked(gate_up, down, x_bf16, T, ids, w, k, residual, out, ws, ws_bytes, stream);
 }
 
 moex_status moex_device_status(moex_stream stream, uint32_t* flags) {

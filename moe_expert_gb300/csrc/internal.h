@@ -50,11 +50,13 @@ moex_status launch_block_dots(const moex_qweight* W, const int8_t* xq, int ncols
 size_t moe_decode_ws_bytes(int T, int k, int64_t hidden, int64_t inter);
 moex_status launch_moe_decode(const moex_qweight* gu, const moex_qweight* dn, const float* x, int T,
                               const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,
-                              float* gu_dbg, float* h_dbg, int8_t* hq_dbg, float* hds_dbg, cudaStream_t s);
+                              float* gu_dbg, float* h_dbg, int8_t* hq_dbg, float* hds_dbg, const float* residual,
+                              cudaStream_t s);
 
 size_t moe_prefill_ws_bytes(int T, int k, int E, int64_t hidden, int64_t inter);
 void prefill_ws_layout(int T, int k, int E, int64_t hidden, int64_t inter, size_t* off);
 moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, const uint16_t* x, int T,
-                               const int32_t* ids, const float* w, int k, float* out, void* ws, cudaStream_t s);
+                               const int32_t* ids, const float* w, int k, const float* residual, float* out, void* ws,
+                               cudaStream_t s);
 
 }  // namespace moex

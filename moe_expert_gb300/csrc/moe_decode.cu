@@ -41,6 +41,7 @@ struct DecodeArgs {
   const int32_t* ids;
   const float* w;
   float* out;
+  const float* residual;  // nullptr, or added to the combine (may equal out)
   int8_t* hq;      // [n][I]
   float* hds;      // [n][I/32][2]
   float* gu_dbg;
@@ -579,7 +580,8 @@ __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
       for (int ks = 1; ks < NS; ++ks) o = o + pr[ks];   // slice order, as the dense GEMV
       acc = __fadd_rn(acc, __fmul_rn(a.w[j], o));
     }
-    a.out[static_cast<int64_t>(t) * a.H + row_begin + rl] = acc;
+    const int64_t o = static_cast<int64_t>(t) * a.H + row_begin + rl;
+    a.out[o] = a.residual ? __fadd_rn(a.residual[o], acc) : acc;
   }
   MOEX_TRACE_STAMP(4);
 }
@@ -652,7 +654,8 @@ moex_status launch_dn_fmt(const DecodeArgs& a, int cap, cudaStream_t s) {
 
 moex_status launch_moe_decode(const moex_qweight* gu, const moex_qweight* dn, const float* x, int T,
                               const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,
-                              float* gu_dbg, float* h_dbg, int8_t* hq_dbg, float* hds_dbg, cudaStream_t s) {
+                              float* gu_dbg, float* h_dbg, int8_t* hq_dbg, float* hds_dbg, const float* residual,
+                              cudaStream_t s) {
   (void)ws_bytes;
   DecodeArgs a = {};
   a.H = static_cast<int>(gu->K);
@@ -673,6 +676,7 @@ moex_status launch_moe_decode(const moex_qweight* gu, const moex_qweight* dn, co
   a.ids = ids;
   a.w = w;
   a.out = out;
+  a.residual = residual;
   a.hq = static_cast<int8_t*>(ws);
   a.hds = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + (static_cast<size_t>(a.n) * a.I + 255) / 256 * 256);
   a.gu_dbg = gu_dbg;

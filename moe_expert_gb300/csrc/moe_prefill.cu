@@ -259,18 +259,19 @@ __global__ void __launch_bounds__(32) prefill_scatter_kernel(const int32_t* __re
 // Xs[p] = fp16(x[token(order[p])]) with each 32-input block interleaved,
 // for the placed rows p < *nrows.  One thread per 32-input block: 64 bytes
 // in, 64 bytes out, all four 16-byte loads issued before any convert.  The
-// same threads clear the layer output (out_vec4 float4s), which the second
-// GEMM accumulates into, so no separate clear sits between the GEMMs.
+// same threads initialise the layer output (out_vec4 float4s), which the
+// second GEMM accumulates into: zeros, or the residual when one is given
+// (which may be out itself), so no separate pass sits between the GEMMs.
 __global__ void __launch_bounds__(256) prefill_gather_kernel(const uint16_t* __restrict__ x, int H, int k,
                                                              const int* __restrict__ nrows,
                                                              const int* __restrict__ order, __half* __restrict__ xs,
-                                                             float4* __restrict__ out, int64_t out_vec4) {
+                                                             const float4* res, float4* out, int64_t out_vec4) {
   pdl_wait();
   pdl_launch_dependents();
   const int per_row = H / QK;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t z = i; z < out_vec4; z += nthreads) out[z] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t z = i; z < out_vec4; z += nthreads) out[z] = res ? res[z] : make_float4(0.f, 0.f, 0.f, 0.f);
   const int64_t row = i / per_row;
   if (row >= *nrows) return;
   const int blk = static_cast<int>(i - row * per_row);
@@ -838,7 +839,8 @@ size_t moe_prefill_ws_bytes(int T, int k, int E, int64_t hidden, int64_t inter) 
 }
 
 moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, const uint16_t* x, int T,
-                               const int32_t* ids, const float* w, int k, float* out, void* ws, cudaStream_t s) {
+                               const int32_t* ids, const float* w, int k, const float* residual, float* out, void* ws,
+                               cudaStream_t s) {
   const int E = gu->n_mats;
   const int H = static_cast<int>(gu->K), I = static_cast<int>(dn->K);
   const int n = T * k;
@@ -884,7 +886,8 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   const int64_t gthreads = static_cast<int64_t>(n) * (H / QK);
   if (launch_pdl(prefill_gather_kernel, dim3(static_cast<unsigned>((gthreads + 255) / 256)), dim3(256), 0, s, x, H,
                  k, static_cast<const int*>(tl.n1 + 2), static_cast<const int*>(order), xs,
-                 reinterpret_cast<float4*>(out), static_cast<int64_t>(T) * H / 4) != cudaSuccess)
+                 reinterpret_cast<const float4*>(residual), reinterpret_cast<float4*>(out),
+                 static_cast<int64_t>(T) * H / 4) != cudaSuccess)
     return MOEX_ECUDA;
   const PfSmem L;
   // pairs share each token stage when both GEMMs have an even number of feature tiles

@@ -119,3 +119,27 @@ def test_strided_output_leaves_padding(fmt, ncols):
     got = to_np(big)
     assert np.array_equal(got[:, :rows].view(np.uint32), y.view(np.uint32))
     assert np.all(np.isnan(got[:, rows:]))
+
+
+# -------------------------------------------------------- vocabulary-sized head
+
+@pytest.mark.parametrize("ncols", [1, 8])
+def test_q8_0_vocab_head_sampled_rows(ncols):
+    """A vocabulary-sized Q8_0 output head, 128256 x 2560 (349 MB of blocks),
+    beyond the register-staged kernel's row limit: every row is computed on
+    the GPU, and the oracle checks 600 sampled rows (first, last, random)."""
+    import torch
+    import moe_expert_gb300 as mx
+    ensure_lib()
+    rows, K = 128256, 2560
+    blocks, x = synth.dense_case("q8_0", rows, K, ncols, seed=31)
+    W = mx.PackedWeight.from_gguf("q8_0", blocks)
+    xq, xds = mx.quantize_q8_1(torch.from_numpy(x).cuda())
+    y = to_np(mx.qgemv(W, xq, xds))
+    assert mx.device_status() == 0
+    rq, rd, _ = oq.quantize_q8_1(x)
+    g = np.random.default_rng(5)
+    sample = np.unique(np.concatenate([[0, 1, rows - 1], g.integers(0, rows, 597)]))
+    ref, A = og.gemv("q8_0", blocks[sample], rq, rd)
+    assert_within(y[:, sample], ref, A, f"q8_0 head c{ncols}")
+    assert np.all(np.isfinite(y))
