@@ -364,6 +364,33 @@ def profiled_traffic(name, sources):
         return None
 
 
+def dense_prefill_detail(reps=10, peak_tflops=None, T=8192, R=12288, K=2560):
+    """Dense prefill product of an IQ4_NL R x K matrix over T BF16 tokens on
+    the tensor cores (tile list + BF16 -> FP16 rows + the GEMM)."""
+    import torch
+    import moe_expert_gb300 as mx
+    blocks, _ = synth.dense_case("iq4_nl", R, K, 1)
+    W = mx.PackedWeight.from_gguf("iq4_nl", blocks)
+    x = torch.from_numpy(synth.prefill_tokens(T, K).view(np.int16)).cuda()
+    y = torch.empty((T, R), dtype=torch.float32, device="cuda")
+    wsb = torch.empty(mx.lib().moex_dense_prefill_workspace_bytes(T, R, K), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        mx.dense_prefill(W, x, y, wsb)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        mx.dense_prefill(W, x, y, wsb)
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / reps
+    flops = 2.0 * T * R * K
+    d = {"tokens": T, "rows": R, "K": K, "ms": round(t * 1e3, 3), "tflops": round(flops / t / 1e12, 1)}
+    if peak_tflops:
+        d["frac_of_fp16_dense_peak"] = round(flops / t / 1e12 / peak_tflops, 3)
+    return d
+
+
 def run_ours(args, ws, rank, local):
     import torch
     import moe_expert_gb300 as mx
@@ -466,6 +493,8 @@ def run_ours(args, ws, rank, local):
         detail["moe_decode_20_experts"] = decode_layer_detail(500)
         torch.cuda.empty_cache()
         detail["moe_prefill_8192_tokens"] = prefill_layer_detail(5, peak_fp16())
+        torch.cuda.empty_cache()
+        detail["dense_prefill_iq4_nl_12288x2560_8192_tokens"] = dense_prefill_detail(10, peak_fp16())
 
     cpu = cpu_baseline(budget_s=args.cpu_budget) if (rank == 0 and not args.no_cpu) else None
     if rank != 0:
@@ -595,6 +624,9 @@ def run_only(args):
         d = prefill_layer_detail(max(1, args.steps), peak_fp16(), args.pf_tokens, args.pf_experts)
         print(json.dumps({"only": "prefill", **d}))
         return
+    elif args.only == "dense_prefill":
+        print(json.dumps({"only": "dense_prefill", **dense_prefill_detail(max(1, args.steps), peak_fp16())}))
+        return
     elif args.only == "decode":
         d = decode_layer_detail(max(1, args.steps))
         print(json.dumps({"only": "decode", **d}))
@@ -614,7 +646,7 @@ def run_only(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--only", default=None, help="profile helper: gemv_q8_0 | gemv_iq4_nl | decode | prefill")
+    ap.add_argument("--only", default=None, help="profile helper: gemv_q8_0 | gemv_iq4_nl | decode | prefill | dense_prefill")
     ap.add_argument("--ncols", type=int, default=1)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)

@@ -231,6 +231,23 @@ moex_status moex_moe_prefill(const moex_qweight* gate_up, const moex_qweight* do
                              const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,
                              moex_stream stream);
 
+/* Workspace bytes of moex_dense_prefill for T tokens and a rows x K matrix. */
+size_t moex_dense_prefill_workspace_bytes(int T, int64_t rows, int64_t K);
+
+/*
+ * Dense prefill product on FP16 tensor cores (#1525 Change: dense weights
+ * dequantised to FP16 for the prompt product, one rounding per value; the
+ * same tcgen05 kernel as the expert GEMMs, on one matrix and every token):
+ *   y[t][r] = sum_i fp16_rn(fp32(d) * kv[r,i]) * fp16_rn(x[t][i])   (FP32 sums)
+ *   W   : IQ4_NL, n_mats == 1, rows % 128 == 0, K % 64 == 0.
+ *   x   : device BF16 bit patterns [T][K], 16-byte aligned.
+ *   y   : device FP32, token t at y + t*ldy (ldy >= rows), fully written.
+ *   ws  : device workspace of moex_dense_prefill_workspace_bytes() bytes.
+ * Three launches (tile list, BF16 -> FP16 rows, the GEMM).
+ */
+moex_status moex_dense_prefill(const moex_qweight* W, const uint16_t* x_bf16, int T, float* y, int64_t ldy, void* ws,
+                               size_t ws_bytes, moex_stream stream);
+
 /*
  * moex_moe_prefill with the residual add fused (#1525 Change): out starts as
  * residual instead of zero, and the second GEMM adds every weighted expert

@@ -64,6 +64,8 @@ SIGNATURES = {
                                                          ctypes.POINTER(_SZ)]),
     "moex_moe_prefill": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _SZ, _P]),
     "moex_moe_decode_noalloc": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P]),
+    "moex_dense_prefill_workspace_bytes": (_SZ, [ctypes.c_int, _I64, _I64]),
+    "moex_dense_prefill": (ctypes.c_int, [_QWP, _P, ctypes.c_int, _P, _I64, _P, _SZ, _P]),
     "moex_moe_decode_residual": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _P, _SZ,
                                                 _P]),
     "moex_moe_prefill_residual": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _P, _SZ,
@@ -308,6 +310,21 @@ def moe_prefill(gate_up: PackedWeight, down: PackedWeight, x_bf16, ids, w, out=N
                                   _ptr(ids), _ptr(w), k, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
            "moex_moe_prefill")
     return out
+
+
+def dense_prefill(W: PackedWeight, x_bf16, y=None, ws=None, stream=None):
+    """Dense prefill product on the tensor cores: y [T, rows] FP32 =
+    fp16(W) . fp16(x)^T for an IQ4_NL matrix and BF16 rows x [T, K]."""
+    torch = _torch()
+    T = x_bf16.shape[0]
+    if y is None:
+        y = torch.empty((T, W.rows), dtype=torch.float32, device=x_bf16.device)
+    if ws is None:
+        ws = torch.empty(lib().moex_dense_prefill_workspace_bytes(T, W.rows, W.K), dtype=torch.uint8,
+                         device=x_bf16.device)
+    _check(lib().moex_dense_prefill(ctypes.byref(W.struct), _ptr(x_bf16), T, _ptr(y), y.stride(0), _ptr(ws), ws.numel(),
+                                    _stream(stream)), "moex_dense_prefill")
+    return y
 
 
 def moe_decode_noalloc(gate_up: PackedWeight, down: PackedWeight, x, ids, w, out=None, stream=None):

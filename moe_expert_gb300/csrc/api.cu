@@ -251,6 +251,23 @@ moex_status moex_moe_prefill_workspace_layout(int T, int k, int E, int64_t hidde
 }
 
 
+size_t moex_dense_prefill_workspace_bytes(int T, int64_t rows, int64_t K) {
+  if (T < 1 || rows < 128 || K < 64) return 0;
+  return dense_prefill_ws_bytes(T, rows, K);
+}
+
+moex_status moex_dense_prefill(const moex_qweight* W, const uint16_t* x_bf16, int T, float* y, int64_t ldy, void* ws,
+                               size_t ws_bytes, moex_stream stream) {
+  const moex_status st = check_weight(W);
+  if (st != MOEX_OK) return st;
+  if (W->fmt != MOEX_IQ4_NL || W->n_mats != 1) return MOEX_EUNSUPPORTED;
+  if (!x_bf16 || !y || !ws || T < 1 || T > (1 << 26) || ldy < W->rows || ldy > INT32_MAX) return MOEX_EINVAL;
+  if (W->rows % 128 != 0 || W->K % 64 != 0 || W->rows > INT32_MAX) return MOEX_EUNSUPPORTED;
+  if (ws_bytes < dense_prefill_ws_bytes(T, W->rows, W->K)) return MOEX_ENOSPACE;
+  if (!aligned16(x_bf16) || !aligned16(ws)) return MOEX_EALIGN;
+  return launch_dense_prefill(W, x_bf16, T, y, ldy, ws, stream);
+}
+
 moex_status moex_moe_prefill(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16, int T,
                              const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,
                              moex_stream stream) {

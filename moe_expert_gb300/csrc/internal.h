@@ -59,4 +59,8 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
                                const int32_t* ids, const float* w, int k, const float* residual, float* out, void* ws,
                                cudaStream_t s);
 
+size_t dense_prefill_ws_bytes(int T, int64_t rows, int64_t K);
+moex_status launch_dense_prefill(const moex_qweight* W, const uint16_t* x, int T, float* y, int64_t ldy, void* ws,
+                                 cudaStream_t s);
+
 }  // namespace moex

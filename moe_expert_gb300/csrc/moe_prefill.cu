@@ -221,6 +221,25 @@ __global__ void __launch_bounds__(256) prefill_tiles_kernel(int E, const int* __
   (first ? tl.t1 : tl.t2)[j] = make_int4(e, f, r0, r1 - r0);
 }
 
+// Dense product: token tiles of 192 rows (the last one ragged) times
+// feature tiles of 128 rows, all of matrix 0; n1[0] = tiles, n1[2] = rows.
+__global__ void __launch_bounds__(256) dense_tiles_kernel(int T, int F, int4* __restrict__ tiles, int* __restrict__ n1) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int ntt = pf_token_tiles(T);
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i == 0) {
+    n1[0] = ntt * F;
+    n1[1] = 0;
+    n1[2] = T;
+    n1[3] = ntt;
+  }
+  if (i >= ntt * F) return;
+  const int tt = i / F, f = i % F;
+  const int r0 = tt * PF_NMAX;
+  tiles[i] = make_int4(0, f, r0, (T - r0) < PF_NMAX ? (T - r0) : PF_NMAX);
+}
+
 // One warp per segment, entries in order, 32 at a time: equal experts are
 // ranked by lane with __match_any_sync; order[row] = entry, tokw[row] =
 // {token, weight bits}.
@@ -275,7 +294,7 @@ __global__ void __launch_bounds__(256) prefill_gather_kernel(const uint16_t* __r
   const int64_t row = i / per_row;
   if (row >= *nrows) return;
   const int blk = static_cast<int>(i - row * per_row);
-  const int t = order[row] / k;
+  const int t = order ? order[row] / k : static_cast<int>(row);  // dense: rows are tokens
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H + blk * QK);
   uint32_t in[16];
 #pragma unroll
@@ -398,6 +417,7 @@ struct PfSmem {
 };
 
 // EPI == 1: SwiGLU -> H (FP16).  EPI == 2: weighted combine into out.
+// EPI == 3: dense product, out[token][feature] = D (FP32, stride Hd).
 // CL == 2: clusters of two CTAs sharing each token stage (multicast); CL == 1: alone.
 template <int EPI, int CL>
 __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __grid_constant__ CUtensorMap bmap,
@@ -683,6 +703,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
             }
             named_bar_sync(4 + pair, 64);
           }
+        } else if (EPI == 3) {
+          const int fo = tile.y * 128 + 32 * q + lane;   // output feature
+          for (int i = 0; i < 32; ++i)
+            if (32 * c + i < tile.w) a.out[static_cast<int64_t>(tile.z + 32 * c + i) * a.Hd + fo] = __uint_as_float(r[i]);
         } else {
           const int fo = tile.y * 128 + 32 * q + lane;   // output feature
           const int pl = 32 * c + lane;
@@ -789,10 +813,11 @@ cudaLaunchConfig_t pf_config(int grid, size_t smem, cudaStream_t s, int cl, cuda
 // when a GPC has an odd number of free SMs.
 int pf_grid(PfKernel kern, int cl, size_t smem) {
   if (cl == 1) return sm_count();
-  static int cached[2] = {0, 0};
-  static PfKernel which[2] = {nullptr, nullptr};
-  for (int i = 0; i < 2; ++i)
-    if (which[i] == kern) return cached[i];
+  static int cached[8] = {};
+  static PfKernel which[8] = {};
+  int slot = 0;
+  for (; slot < 8 && which[slot]; ++slot)
+    if (which[slot] == kern) return cached[slot];
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pf_config(sm_count(), smem, nullptr, cl, attr);
   int nclusters = 0;
@@ -800,7 +825,7 @@ int pf_grid(PfKernel kern, int cl, size_t smem) {
     cudaGetLastError();
     nclusters = sm_count() / 2;
   }
-  const int slot = which[0] == nullptr ? 0 : 1;
+  if (slot == 8) return 2 * nclusters;
   which[slot] = kern;
   cached[slot] = 2 * nclusters;
   return cached[slot];
@@ -924,6 +949,63 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   g2.tokw = tokw;
   g2.status = status;
   if (launch_pf_gemm(k2, cl, L.total, s, m2, q2, s2, g2) != cudaSuccess) return MOEX_ECUDA;
+  return MOEX_OK;
+}
+
+// Dense prefill workspace: tiles, totals, Xs.
+void dense_ws_layout(int T, int64_t rows, int64_t K, size_t* off) {
+  const size_t tiles = static_cast<size_t>(pf_token_tiles(T)) * static_cast<size_t>(rows / 128);
+  size_t o = 0;
+  off[0] = o; o = align_up(o + 16 * tiles, 256);                     // tiles
+  off[1] = o; o = align_up(o + 16, 256);                             // totals
+  off[2] = o; o = align_up(o + 2 * static_cast<size_t>(T) * K, 256); // Xs
+  off[3] = o;
+}
+
+size_t dense_prefill_ws_bytes(int T, int64_t rows, int64_t K) {
+  size_t off[4];
+  dense_ws_layout(T, rows, K, off);
+  return off[3];
+}
+
+moex_status launch_dense_prefill(const moex_qweight* W, const uint16_t* x, int T, float* y, int64_t ldy, void* ws,
+                                 cudaStream_t s) {
+  const int K = static_cast<int>(W->K);
+  const int F = static_cast<int>(W->rows / 128);
+  size_t off[4];
+  dense_ws_layout(T, W->rows, K, off);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  int4* tiles = reinterpret_cast<int4*>(wsb + off[0]);
+  int* n1 = reinterpret_cast<int*>(wsb + off[1]);
+  __half* xs = reinterpret_cast<__half*>(wsb + off[2]);
+  uint32_t* status = device_status_ptr();
+  CUtensorMap bm, qm, sm;
+  if (!make_map(&bm, xs, T, K) || !make_weight_maps(&qm, &sm, W)) return MOEX_ECUDA;
+  const int ntiles = pf_token_tiles(T) * F;
+  if (launch_pdl(dense_tiles_kernel, dim3((ntiles + 255) / 256), dim3(256), 0, s, T, F, tiles, n1) != cudaSuccess)
+    return MOEX_ECUDA;
+  const int64_t gthreads = static_cast<int64_t>(T) * (K / QK);
+  if (launch_pdl(prefill_gather_kernel, dim3(static_cast<unsigned>((gthreads + 255) / 256)), dim3(256), 0, s, x, K, 1,
+                 static_cast<const int*>(n1 + 2), static_cast<const int*>(nullptr), xs,
+                 static_cast<const float4*>(nullptr), static_cast<float4*>(nullptr), int64_t(0)) != cudaSuccess)
+    return MOEX_ECUDA;
+  const PfSmem L;
+  const int cl = F % 2 == 0 ? 2 : 1;
+  const PfKernel kern = cl == 2 ? prefill_gemm_kernel<3, 2> : prefill_gemm_kernel<3, 1>;
+  if (ensure_smem(reinterpret_cast<const void*>(kern), L.total) != cudaSuccess) return MOEX_ECUDA;
+  GemmArgs g = {};
+  g.qs = static_cast<const uint8_t*>(W->qs);
+  g.sc = static_cast<const uint8_t*>(W->scales);
+  g.qrow = static_cast<int>(qs_row_bytes(W->fmt, W->K));
+  g.scrow = static_cast<int>(sc_row_bytes(W->K));
+  g.rows_per_expert = W->rows;
+  g.K = K;
+  g.tiles = tiles;
+  g.ntiles = n1;
+  g.out = y;
+  g.Hd = static_cast<int>(ldy);
+  g.status = status;
+  if (launch_pf_gemm(kern, cl, L.total, s, bm, qm, sm, g) != cudaSuccess) return MOEX_ECUDA;
   return MOEX_OK;
 }
 

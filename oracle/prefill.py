@@ -69,6 +69,21 @@ class ExpertCache:
         return self.cache[e].astype(np.float64)
 
 
+def dense_prefill(blocks, x_bf16: np.ndarray, fmt: str = "iq4_nl", rows=None):
+    """The dense prefill product (#1525 Change: dense weights dequantised to
+    FP16 for the prompt product, one rounding per value, FP32 sums; here
+    the sums are float64): y[t][r] = sum_i Wh[r, i] * Xh[t, i] with
+    Wh = fp16_rn(fp32(d) * kv) and Xh = fp16_rn(bf16 x).
+
+    blocks: GGUF blocks [R, K/32, *]; ``rows`` restricts the output to those
+    weight rows.  Returns (y [T, len(rows)] float64, error scale
+    A = |Wh| . |Xh|^T)."""
+    b = blocks if rows is None else blocks[np.asarray(rows)]
+    wh = dequant_fp16(fmt, b).astype(np.float64)
+    xh = fp16_rn(bf16_bits_to_f32(x_bf16)).astype(np.float64)
+    return xh @ wh.T, np.abs(xh) @ np.abs(wh).T
+
+
 def moe_prefill(gate_up, down, x_bf16: np.ndarray, ids: np.ndarray, w: np.ndarray,
                 tokens=None, fmt: str = "iq4_nl", h_override=None):
     """Prefill output rows for ``tokens`` (default: every token).

@@ -474,3 +474,33 @@ def test_planted_transposed_gate_up_is_caught(monkeypatch):
     monkeypatch.setattr(moe, "swiglu", lambda gu, inter: moe.silu(gu[..., inter:]) * gu[..., :inter])
     with pytest.raises(AssertionError):
         test_swiglu_split_layout()
+
+
+def test_dense_prefill_one_hot_rows_and_brute_force():
+    """The dense prefill oracle: a one-hot token row (x = 1 at input i)
+    returns column i of the FP16 weights exactly; a tiny case equals a plain
+    triple loop over the FP16 roundings of each weight and input."""
+    g = synth.rng(41)
+    R, K = 4, 64
+    blocks = synth.iq4_nl_blocks(g, R, K)
+    one = np.uint16(0x3F80)                     # BF16 1.0
+    x = np.zeros((3, K), dtype=np.uint16)
+    for t, i in enumerate([0, 17, 63]):
+        x[t, i] = one
+    y, _ = prefill.dense_prefill(blocks, x)
+    wh = prefill.dequant_fp16("iq4_nl", blocks).astype(np.float64)
+    for t, i in enumerate([0, 17, 63]):
+        assert np.array_equal(y[t], wh[:, i])
+    xb = synth.bf16_activations(g, 3, K)
+    y, A = prefill.dense_prefill(blocks, xb)
+    d, q = formats.decode("iq4_nl", blocks)
+    for t in range(3):
+        for r in range(R):
+            acc = 0.0
+            for i in range(K):
+                wv = float(np.float16(np.float32(d[r, i // 32]) * np.float32(q[r, i])))
+                xv = float(np.float16(np.uint32(int(xb[t, i]) << 16).view(np.float32)))
+                acc += wv * xv
+            assert abs(acc - y[t, r]) <= 1e-12 * max(1.0, A[t, r])
+    y2, _ = prefill.dense_prefill(blocks, xb, rows=[2, 0])
+    assert np.array_equal(y2, y[:, [2, 0]])
