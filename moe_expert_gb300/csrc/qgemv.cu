@@ -358,8 +358,9 @@ moex_status launch_c(const GemvArgs& a, int smem_cap, cudaStream_t s) {
     // slice, two CTAs per SM (the next GEMV overlaps this one's drain); more
     // columns are compute-bound: one CTA per SM with twice the warps, the
     // columns split over two warp groups
+    // (IQ4_NL keeps one column group: a second would decode every block twice)
     if constexpr (C <= 4) return launch_one<FMT, C, 2, 2>(a, smem_cap, s);
-    else if constexpr (C % 2 == 0) return launch_one<FMT, C, 2, 1, 2>(a, smem_cap, s);
+    else if constexpr (C % 2 == 0 && FMT == MOEX_Q8_0) return launch_one<FMT, C, 2, 1, 2>(a, smem_cap, s);
     else return launch_one<FMT, C, 2, 1>(a, smem_cap, s);
   }
   return launch_one<FMT, C, 1, 1>(a, smem_cap, s);
