@@ -215,17 +215,20 @@ moex_status moex_moe_prefill_workspace_layout(int T, int k, int E, int64_t hidde
  * FP32 sums; #1525 Change: one rounding per dequantised value, SwiGLU
  * between the products, the top-k combine):
  *   rows sorted by expert (stable), Xs = fp16(x), Wh = fp16_rn(d * kvalue)
+ *   (IQ4_NL) or fp16_rn(d * q) (Q8_0)
  *   H  = fp16(silu(g) * u),  g, u = Wh_gu[e] . Xs   (FP32 accumulation)
  *   out[t] = sum_k w[t,k] * (Wh_dn[e] . H)          (FP32, summed with
  *            atomic adds: the order of the k terms is not fixed)
- *   gate_up, down : IQ4_NL stacks [E][2*inter][hidden], [E][hidden][inter].
+ *   gate_up, down : IQ4_NL or Q8_0 stacks (each its own format)
+ *            [E][2*inter][hidden], [E][hidden][inter].
  *   x_bf16 : device BF16 [T][hidden];  ids, w : device [T][k] (from
  *            moex_route_topk); out : device FP32 [T][hidden] (overwritten).
  *   ws     : device workspace of moex_moe_prefill_workspace_bytes() bytes.
  * hidden % 128 == 0, inter % 64 == 0, E <= 4096, E * 2 * inter < 2^31.
  * Seven launches (sort: histogram, scan, tiles, scatter; gather, which also
- * clears out; GEMM 1; GEMM 2); the GEMMs use tcgen05 / TMEM / TMA.  An entry whose id is
- * outside [0, E) is left out of the layer and flagged (MOEX_EDEVICE).
+ * clears out; GEMM 1; GEMM 2); the GEMMs use tcgen05 / TMEM / TMA.  An
+ * entry whose id is outside [0, E) is left out of the layer and flagged
+ * (MOEX_EDEVICE).
  */
 moex_status moex_moe_prefill(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16, int T,
                              const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,
@@ -239,7 +242,7 @@ size_t moex_dense_prefill_workspace_bytes(int T, int64_t rows, int64_t K);
  * dequantised to FP16 for the prompt product, one rounding per value; the
  * same tcgen05 kernel as the expert GEMMs, on one matrix and every token):
  *   y[t][r] = sum_i fp16_rn(fp32(d) * kv[r,i]) * fp16_rn(x[t][i])   (FP32 sums)
- *   W   : IQ4_NL, n_mats == 1, rows % 128 == 0, K % 64 == 0.
+ *   W   : IQ4_NL or Q8_0, n_mats == 1, rows % 128 == 0, K % 64 == 0.
  *   x   : device BF16 bit patterns [T][K], 16-byte aligned.
  *   y   : device FP32, token t at y + t*ldy (ldy >= rows), fully written.
  *   ws  : device workspace of moex_dense_prefill_workspace_bytes() bytes.

@@ -102,7 +102,7 @@ moex_status prefill_checked(const moex_qweight* gate_up, const moex_qweight* dow
   if (st != MOEX_OK) return st;
   st = check_weight(down);
   if (st != MOEX_OK) return st;
-  if (gate_up->fmt != MOEX_IQ4_NL || down->fmt != MOEX_IQ4_NL) return MOEX_EUNSUPPORTED;
+
   if (!x_bf16 || !ids || !w || !out || !ws) return MOEX_EINVAL;
   if (T < 1 || k < 1 || k > 16 || static_cast<int64_t>(T) * k > (int64_t(1) << 26)) return MOEX_EINVAL;
   if (gate_up->n_mats != down->n_mats || gate_up->n_mats > 4096) return MOEX_EINVAL;
@@ -260,7 +260,7 @@ moex_status moex_dense_prefill(const moex_qweight* W, const uint16_t* x_bf16, in
                                size_t ws_bytes, moex_stream stream) {
   const moex_status st = check_weight(W);
   if (st != MOEX_OK) return st;
-  if (W->fmt != MOEX_IQ4_NL || W->n_mats != 1) return MOEX_EUNSUPPORTED;
+  if (W->n_mats != 1) return MOEX_EUNSUPPORTED;
   if (!x_bf16 || !y || !ws || T < 1 || T > (1 << 26) || ldy < W->rows || ldy > INT32_MAX) return MOEX_EINVAL;
   if (W->rows % 128 != 0 || W->K % 64 != 0 || W->rows > INT32_MAX) return MOEX_EUNSUPPORTED;
   if (ws_bytes < dense_prefill_ws_bytes(T, W->rows, W->K)) return MOEX_ENOSPACE;

@@ -57,10 +57,11 @@ constexpr int PF_EPI0 = PF_DQ0 + PF_DQ_WARPS;           // first epilogue warp
 // Raw weight stages: the IQ4_NL bytes of 128 rows x 4 k-steps (8 blocks a
 // row), two boxes of 64 rows x 128 bytes with the 128-byte swizzle, then
 // their FP16 scales, two boxes of 64 rows x 16 bytes.
-constexpr int PF_RAW_KS = 4;                      // k-steps per raw stage
+constexpr int PF_RAW_KS = 4;                      // k-steps per IQ4_NL raw stage (Q8_0: 2, same bytes)
 constexpr int PF_NR_ST = 4;                       // raw stages
 constexpr int PF_RAW_QS = 128 * 128;              // nibble bytes of a raw stage
 constexpr int PF_RAW_STAGE = PF_RAW_QS + 128 * 16;  // + scale bytes (multiple of 1024)
+__host__ __device__ constexpr int pf_raw_ks(int wf) { return wf == MOEX_Q8_0 ? 2 : PF_RAW_KS; }
 
 // ----------------------------------------------------------------- sort
 
@@ -382,6 +383,33 @@ __device__ __forceinline__ void dequant_block16(uint4 n, uint16_t dbits, uint32_
   }
 }
 
+// Dequantises one Q8_0 block (32 int8 q in two 16-byte halves lo = q[0..15],
+// hi = q[16..31], FP16 scale d) into the same 16 TMEM column words as
+// dequant_block16: word j = half2(d * q[j], d * q[j+16]), each product
+// rounded once to FP16.  The byte q + 128 becomes the FP16 1024 + q + 128
+// exactly (0x6400 | byte), minus 1152 gives q.
+__device__ __forceinline__ void dequant_q8_block16(uint4 lo, uint4 hi, uint16_t dbits, uint32_t (&col)[16]) {
+  const __half2 one152 = __half2half2(__ushort_as_half(0x6480));  // 1152
+  const __half2 d2 = __half2half2(__ushort_as_half(dbits));
+  const uint32_t L[4] = {lo.x, lo.y, lo.z, lo.w}, H[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    // [q4i, q4i+16, q4i+1, q4i+17] and [q4i+2, q4i+18, q4i+3, q4i+19], biased by 128
+    const uint32_t u01 = prmt(L[i], H[i], 0x5140u) ^ 0x80808080u;
+    const uint32_t u23 = prmt(L[i], H[i], 0x7362u) ^ 0x80808080u;
+    const uint32_t U[2] = {u01, u23};
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const uint32_t p0 = prmt(U[hh], 0x64646464u, 0x4140u);
+      const uint32_t p1 = prmt(U[hh], 0x64646464u, 0x4342u);
+      __half2 h0 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p0), one152), d2);
+      __half2 h1 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p1), one152), d2);
+      col[4 * i + 2 * hh] = *reinterpret_cast<uint32_t*>(&h0);
+      col[4 * i + 2 * hh + 1] = *reinterpret_cast<uint32_t*>(&h1);
+    }
+  }
+}
+
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
@@ -418,8 +446,9 @@ struct PfSmem {
 
 // EPI == 1: SwiGLU -> H (FP16).  EPI == 2: weighted combine into out.
 // EPI == 3: dense product, out[token][feature] = D (FP32, stride Hd).
+// WF: the weight format, IQ4_NL (raw stages of 4 k-steps) or Q8_0 (2).
 // CL == 2: clusters of two CTAs sharing each token stage (multicast); CL == 1: alone.
-template <int EPI, int CL>
+template <int EPI, int CL, int WF>
 __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __grid_constant__ CUtensorMap bmap,
                                                                      const __grid_constant__ CUtensorMap qmap,
                                                                      const __grid_constant__ CUtensorMap smap,
@@ -573,7 +602,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
     // ------------------------------------------------ A producer (TMA of the raw weight bytes)
     if (lane == 0) {
       int rc = 0;
-      const int ngroups = (KS + PF_RAW_KS - 1) / PF_RAW_KS;
+      constexpr int RKS = pf_raw_ks(WF);
+      const int ngroups = (KS + RKS - 1) / RKS;
       int4 nxt = t0 < ntiles ? a.tiles[t0] : make_int4(0, 0, 0, 0);
       for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
         const int4 tile = nxt;
@@ -593,8 +623,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
           mbar_arrive_expect_tx(&r_full[r], PF_RAW_STAGE);
           tma_load_2d(st, &qmap, g * 128, y0, &r_full[r]);
           tma_load_2d(st + 64 * 128, &qmap, g * 128, y1, &r_full[r]);
-          tma_load_2d(st + PF_RAW_QS, &smap, g * 16, y0, &r_full[r]);
-          tma_load_2d(st + PF_RAW_QS + 64 * 16, &smap, g * 16, y1, &r_full[r]);
+          // scales: 16 bytes = 4 k-steps (a Q8_0 stage of 2 k-steps takes half of it)
+          const int sx = (WF == MOEX_Q8_0 ? g >> 1 : g) * 16;
+          tma_load_2d(st + PF_RAW_QS, &smap, sx, y0, &r_full[r]);
+          tma_load_2d(st + PF_RAW_QS + 64 * 16, &smap, sx, y1, &r_full[r]);
         }
       }
       if (*abort_flag) {
@@ -612,7 +644,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
     // this row's bytes in a raw stage: 128-byte rows, 16-byte chunk c stored at chunk c ^ (row & 7)
     const int qoff = (m >> 6) * 64 * 128 + (m & 63) * 128;
     const int soff = PF_RAW_QS + (m >> 6) * 64 * 16 + (m & 63) * 16;
-    const int ngroups = (KS + PF_RAW_KS - 1) / PF_RAW_KS;
+    constexpr int RKS = pf_raw_ks(WF);
+    const int ngroups = (KS + RKS - 1) / RKS;
     int kc = 0, rc = 0;
     for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
       for (int g = 0; g < ngroups && !*abort_flag; ++g, ++rc) {
@@ -623,22 +656,31 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
           break;
         }
         const uint8_t* st = sraw + r * PF_RAW_STAGE;
-        const int nk = min(PF_RAW_KS, KS - g * PF_RAW_KS);
+        const int nk = min(RKS, KS - g * RKS);
         const uint4 scv = *reinterpret_cast<const uint4*>(st + soff);
-        uint4 qv[PF_RAW_KS];
+        // block 2j + h of the stage: IQ4_NL 16 bytes (chunk 2j + h), Q8_0 32 bytes (chunks 2(2j + h), +1)
+        constexpr int NCH = WF == MOEX_Q8_0 ? 2 : 1;
+        uint4 qv[RKS][NCH];
 #pragma unroll
-        for (int j = 0; j < PF_RAW_KS; ++j)
-          if (j < nk) qv[j] = *reinterpret_cast<const uint4*>(st + qoff + (((2 * j + h) ^ (m & 7)) << 4));
+        for (int j = 0; j < RKS; ++j)
+#pragma unroll
+          for (int c = 0; c < NCH; ++c)
+            if (j < nk) qv[j][c] = *reinterpret_cast<const uint4*>(st + qoff + (((NCH * (2 * j + h) + c) ^ (m & 7)) << 4));
         __syncwarp();
         if (lane == 0) mbar_arrive(&r_empty[r]);  // the raw bytes are in registers
         const uint32_t sw[4] = {scv.x, scv.y, scv.z, scv.w};
 #pragma unroll
-        for (int j = 0; j < PF_RAW_KS; ++j) {
+        for (int j = 0; j < RKS; ++j) {
           if (j >= nk) break;
-          // scale of block 2j + h of the group: 16-bit half h of word j
-          const uint16_t dbits = static_cast<uint16_t>(h ? (sw[j] >> 16) : (sw[j] & 0xFFFFu));
+          // scale of block 2k + h of the 4 k-steps the 16 scale bytes cover: 16-bit half h of word k
+          uint32_t swv = sw[j];
+          if (WF == MOEX_Q8_0 && (g & 1)) swv = sw[j + 2 < 4 ? j + 2 : 3];
+          const uint16_t dbits = static_cast<uint16_t>(h ? (swv >> 16) : (swv & 0xFFFFu));
           uint32_t col[16];
-          dequant_block16(qv[j], dbits, col);
+          if constexpr (WF == MOEX_Q8_0)
+            dequant_q8_block16(qv[j][0], qv[j][NCH - 1], dbits, col);
+          else
+            dequant_block16(qv[j][0], dbits, col);
           const int s = kc % PF_NA_ST;
           if (kc >= PF_NA_ST && !mbar_wait(&ab_empty[s], ((kc / PF_NA_ST) - 1) & 1, abort_flag)) {
             *abort_flag = 1;
@@ -779,11 +821,13 @@ bool make_plane_map(CUtensorMap* m, const void* base, int64_t rows, int64_t used
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Nibble map (box 128 bytes = 4 k-steps, 128-byte swizzle) and scale map
-// (box 16 bytes = the 8 scales of the same 4 k-steps) of a weight stack.
+// Quant map (box 128 bytes: 4 IQ4_NL k-steps or 2 Q8_0 k-steps, 128-byte
+// swizzle) and scale map (box 16 bytes = the 8 scales of 4 k-steps) of a
+// weight stack.
 bool make_weight_maps(CUtensorMap* qm, CUtensorMap* sm, const moex_qweight* w) {
   const int64_t rows = static_cast<int64_t>(w->n_mats) * w->rows;
-  return make_plane_map(qm, w->qs, rows, w->K / 2, qs_row_bytes(w->fmt, w->K), 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+  const int64_t qused = w->fmt == MOEX_Q8_0 ? w->K : w->K / 2;  // quant bytes of a row
+  return make_plane_map(qm, w->qs, rows, qused, qs_row_bytes(w->fmt, w->K), 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_plane_map(sm, w->scales, rows, w->K / 16, sc_row_bytes(w->K), 16, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
@@ -829,6 +873,12 @@ int pf_grid(PfKernel kern, int cl, size_t smem) {
   which[slot] = kern;
   cached[slot] = 2 * nclusters;
   return cached[slot];
+}
+
+template <int EPI>
+PfKernel pf_kernel(int cl, int fmt) {
+  if (fmt == MOEX_Q8_0) return cl == 2 ? prefill_gemm_kernel<EPI, 2, MOEX_Q8_0> : prefill_gemm_kernel<EPI, 1, MOEX_Q8_0>;
+  return cl == 2 ? prefill_gemm_kernel<EPI, 2, MOEX_IQ4_NL> : prefill_gemm_kernel<EPI, 1, MOEX_IQ4_NL>;
 }
 
 cudaError_t launch_pf_gemm(PfKernel kern, int cl, size_t smem, cudaStream_t s, const CUtensorMap& bmap,
@@ -917,8 +967,8 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   const PfSmem L;
   // pairs share each token stage when both GEMMs have an even number of feature tiles
   const int cl = (tl.F1 % 2 == 0 && tl.F2 % 2 == 0) ? 2 : 1;
-  const PfKernel k1 = cl == 2 ? prefill_gemm_kernel<1, 2> : prefill_gemm_kernel<1, 1>;
-  const PfKernel k2 = cl == 2 ? prefill_gemm_kernel<2, 2> : prefill_gemm_kernel<2, 1>;
+  const PfKernel k1 = pf_kernel<1>(cl, gu->fmt);
+  const PfKernel k2 = pf_kernel<2>(cl, dn->fmt);
   if (ensure_smem(reinterpret_cast<const void*>(k1), L.total) != cudaSuccess ||
       ensure_smem(reinterpret_cast<const void*>(k2), L.total) != cudaSuccess)
     return MOEX_ECUDA;
@@ -991,7 +1041,7 @@ moex_status launch_dense_prefill(const moex_qweight* W, const uint16_t* x, int T
     return MOEX_ECUDA;
   const PfSmem L;
   const int cl = F % 2 == 0 ? 2 : 1;
-  const PfKernel kern = cl == 2 ? prefill_gemm_kernel<3, 2> : prefill_gemm_kernel<3, 1>;
+  const PfKernel kern = pf_kernel<3>(cl, W->fmt);
   if (ensure_smem(reinterpret_cast<const void*>(kern), L.total) != cudaSuccess) return MOEX_ECUDA;
   GemmArgs g = {};
   g.qs = static_cast<const uint8_t*>(W->qs);

@@ -85,7 +85,7 @@ def dense_prefill(blocks, x_bf16: np.ndarray, fmt: str = "iq4_nl", rows=None):
 
 
 def moe_prefill(gate_up, down, x_bf16: np.ndarray, ids: np.ndarray, w: np.ndarray,
-                tokens=None, fmt: str = "iq4_nl", h_override=None):
+                tokens=None, fmt: str = "iq4_nl", h_override=None, down_fmt=None):
     """Prefill output rows for ``tokens`` (default: every token).
 
     gate_up[e]: GGUF blocks [2*inter, hidden/32, *]; down[e]: [hidden, inter/32, *].
@@ -100,7 +100,7 @@ def moe_prefill(gate_up, down, x_bf16: np.ndarray, ids: np.ndarray, w: np.ndarra
     if tokens is None:
         tokens = list(range(T))
     Wgu = ExpertCache(fmt, gate_up)
-    Wdn = ExpertCache(fmt, down)
+    Wdn = ExpertCache(down_fmt or fmt, down)
     inter = Wgu[int(ids[tokens[0], 0])].shape[0] // 2
     n = len(tokens)
     out = np.zeros((n, hidden))

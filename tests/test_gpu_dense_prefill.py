@@ -52,3 +52,24 @@ def test_dense_prefill_full_size_sampled():
     ref, A = op.dense_prefill(blocks, xb[toks], rows=rows)
     assert_within(y[np.ix_(toks, rows)], ref, A, "dense 8192x12288x2560")
     assert np.all(np.isfinite(y))
+
+
+def _run_fmt(fmt, T, R, K, seed):
+    import torch
+    import moe_expert_gb300 as mx
+    ensure_lib()
+    g = synth.rng(seed)
+    blocks = synth.weight_blocks(fmt, g, R, K)
+    xb = synth.bf16_activations(g, T, K)
+    W = mx.PackedWeight.from_gguf(fmt, blocks)
+    y = to_np(mx.dense_prefill(W, torch.from_numpy(xb.view(np.int16)).cuda()))
+    assert mx.device_status() == 0
+    return blocks, xb, y
+
+
+@pytest.mark.parametrize("T,R,K", [(300, 256, 512), (193, 384, 1536), (70, 128, 192)])
+def test_dense_prefill_q8_0(T, R, K):
+    """Q8_0 weights: raw stages of two k-steps, Wh = fp16_rn(d * q)."""
+    blocks, xb, y = _run_fmt("q8_0", T, R, K, seed=T * 3 + R)
+    ref, A = op.dense_prefill(blocks, xb, fmt="q8_0")
+    assert_within(y, ref, A, f"dense q8_0 {T}x{R}x{K}")

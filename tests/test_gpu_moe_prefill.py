@@ -30,20 +30,20 @@ def deinterleave(a):
     return np.concatenate([b[..., 0], b[..., 1]], axis=2).reshape(r, K)
 
 
-def build(E, hidden, inter, experts, seed):
+def build(E, hidden, inter, experts, seed, gu_fmt="iq4_nl"):
     import moe_expert_gb300 as mx
-    gu = mx.PackedWeight("iq4_nl", E, 2 * inter, hidden).zero_()
+    gu = mx.PackedWeight(gu_fmt, E, 2 * inter, hidden).zero_()
     dn = mx.PackedWeight("iq4_nl", E, hidden, inter).zero_()
     gub, dnb = {}, {}
     for e in sorted(set(int(v) for v in experts)):
-        gub[e] = synth.expert_blocks("gate_up", e, hidden, inter, "iq4_nl", seed=seed)
+        gub[e] = synth.expert_blocks("gate_up", e, hidden, inter, gu_fmt, seed=seed)
         dnb[e] = synth.expert_blocks("down", e, hidden, inter, "iq4_nl", seed=seed)
         gu.pack_matrix(e, gub[e])
         dn.pack_matrix(e, dnb[e])
     return gu, dn, gub, dnb
 
 
-def run(T, E, k, hidden, inter, seed, sample=None):
+def run(T, E, k, hidden, inter, seed, sample=None, gu_fmt="iq4_nl"):
     import torch
     import moe_expert_gb300 as mx
     ensure_lib()
@@ -54,7 +54,7 @@ def run(T, E, k, hidden, inter, seed, sample=None):
     ids, w = to_np(ids_t), to_np(w_t)
     rid, rw = om.route_topk(logits, k)
     assert np.array_equal(ids.astype(np.int64), rid)
-    gu, dn, gub, dnb = build(E, hidden, inter, ids.reshape(-1), seed)
+    gu, dn, gub, dnb = build(E, hidden, inter, ids.reshape(-1), seed, gu_fmt)
     xt = torch.from_numpy(xb.view(np.int16)).cuda()
     ws = torch.zeros(mx.moe_prefill_workspace_bytes(T, k, E, hidden, inter), dtype=torch.uint8, device="cuda")
     out = to_np(mx.moe_prefill(gu, dn, xt, ids_t, w_t, ws=ws))
@@ -80,8 +80,10 @@ def run(T, E, k, hidden, inter, seed, sample=None):
     Hfull = wsh[off[7]:off[7] + 2 * n * inter].view(np.float16).reshape(n, inter)
     toks = list(range(T)) if sample is None else list(sample)
     gpu_h = lambda t, s: deinterleave(Hfull[pos[t * k + s]][None, :])[0]  # noqa: E731
-    ref = op.moe_prefill(gub, dnb, xb, ids, w.astype(np.float64), tokens=toks, h_override=gpu_h)
-    own = op.moe_prefill(gub, dnb, xb, ids, w.astype(np.float64), tokens=toks)
+    ref = op.moe_prefill(gub, dnb, xb, ids, w.astype(np.float64), tokens=toks, h_override=gpu_h,
+                           fmt=gu_fmt, down_fmt="iq4_nl")
+    own = op.moe_prefill(gub, dnb, xb, ids, w.astype(np.float64), tokens=toks, fmt=gu_fmt,
+                           down_fmt="iq4_nl")
     Hg = ref["H"].astype(np.float64)
     Hr = own["H"].astype(np.float64)
     ulp = np.abs(np.spacing(own["H"].astype(np.float16)).astype(np.float64))
@@ -107,6 +109,12 @@ def run(T, E, k, hidden, inter, seed, sample=None):
 ])
 def test_prefill_small(T, E, k, hidden, inter):
     mism, worst = run(T, E, k, hidden, inter, seed=T + E)
+    print(f"H mismatches {mism:.2e}, worst out error / tolerance {worst:.3f}")
+
+
+def test_prefill_q8_0_gate_up():
+    """Q8_0 gate/up (the decode layer's format) with IQ4_NL down."""
+    mism, worst = run(300, 8, 2, 512, 128, seed=91, gu_fmt="q8_0")
     print(f"H mismatches {mism:.2e}, worst out error / tolerance {worst:.3f}")
 
 

@@ -504,3 +504,25 @@ def test_dense_prefill_one_hot_rows_and_brute_force():
             assert abs(acc - y[t, r]) <= 1e-12 * max(1.0, A[t, r])
     y2, _ = prefill.dense_prefill(blocks, xb, rows=[2, 0])
     assert np.array_equal(y2, y[:, [2, 0]])
+
+
+def test_dequant_fp16_q8_0_codes_and_scales():
+    """fp16_rn(d * q) for Q8_0: every int8 code of a block set (-128..127
+    over 8 blocks) at zero / subnormal / normal / huge scales, against exact
+    rationals rounded by Python's own FP16 packer."""
+    scale_bits = [0x0000, 0x0001, 0x03FF, 0x2E66, 0x3C00, 0x5640, 0x7BFF]
+    codes = np.arange(-128, 128, dtype=np.int16).astype(np.int8).reshape(8, 32)
+    for sb in scale_bits:
+        blocks = np.zeros((1, 8, 34), dtype=np.uint8)
+        blocks[0, :, 0] = sb & 0xFF
+        blocks[0, :, 1] = sb >> 8
+        blocks[0, :, 2:34] = codes.view(np.uint8)
+        got = prefill.dequant_fp16("q8_0", blocks).reshape(-1)
+        d = _fp16_exact(sb)
+        for i, q in enumerate(codes.reshape(-1)):
+            exact = float(d * int(q))
+            try:
+                want = struct.unpack("<e", struct.pack("<e", exact))[0]
+            except OverflowError:
+                want = math.copysign(math.inf, exact)
+            assert float(got[i]) == want or (math.isinf(want) and math.isinf(float(got[i])))
