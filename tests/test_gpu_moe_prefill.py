@@ -43,17 +43,22 @@ def build(E, hidden, inter, experts, seed, gu_fmt="iq4_nl"):
     return gu, dn, gub, dnb
 
 
-def run(T, E, k, hidden, inter, seed, sample=None, gu_fmt="iq4_nl"):
+def run(T, E, k, hidden, inter, seed, sample=None, gu_fmt="iq4_nl", routing=None):
     import torch
     import moe_expert_gb300 as mx
     ensure_lib()
     xb = synth.bf16_activations(synth.rng(seed), T, hidden)
-    logits = synth.router_logits(synth.rng(seed + 1), T, E)
-    lt = torch.from_numpy(logits).cuda()
-    ids_t, w_t = mx.route_topk(lt, k)
-    ids, w = to_np(ids_t), to_np(w_t)
-    rid, rw = om.route_topk(logits, k)
-    assert np.array_equal(ids.astype(np.int64), rid)
+    if routing is None:
+        logits = synth.router_logits(synth.rng(seed + 1), T, E)
+        lt = torch.from_numpy(logits).cuda()
+        ids_t, w_t = mx.route_topk(lt, k)
+        ids, w = to_np(ids_t), to_np(w_t)
+        rid, rw = om.route_topk(logits, k)
+        assert np.array_equal(ids.astype(np.int64), rid)
+    else:
+        ids, w = routing
+        ids_t = torch.from_numpy(ids.astype(np.int32)).cuda()
+        w_t = torch.from_numpy(w.astype(np.float32)).cuda()
     gu, dn, gub, dnb = build(E, hidden, inter, ids.reshape(-1), seed, gu_fmt)
     xt = torch.from_numpy(xb.view(np.int16)).cuda()
     ws = torch.zeros(mx.moe_prefill_workspace_bytes(T, k, E, hidden, inter), dtype=torch.uint8, device="cuda")
@@ -109,6 +114,20 @@ def run(T, E, k, hidden, inter, seed, sample=None, gu_fmt="iq4_nl"):
 ])
 def test_prefill_small(T, E, k, hidden, inter):
     mism, worst = run(T, E, k, hidden, inter, seed=T + E)
+    print(f"H mismatches {mism:.2e}, worst out error / tolerance {worst:.3f}")
+
+
+def test_prefill_expert_count_boundaries():
+    """Experts with 0, 1, 192, 193, 384 and 130 rows (k = 1): an empty
+    expert, a one-row tile, exactly one full tile, one row over, two full
+    tiles, and a ragged single tile; the routing is given, not drawn."""
+    counts = [0, 1, 192, 193, 384, 130]
+    E, T = len(counts), sum(counts)
+    g = np.random.default_rng(17)
+    ids = np.repeat(np.arange(E), counts)
+    g.shuffle(ids)
+    w = g.uniform(0.2, 1.0, size=T).astype(np.float32)
+    mism, worst = run(T, E, 1, 256, 64, seed=29, routing=(ids.reshape(T, 1), w.reshape(T, 1)))
     print(f"H mismatches {mism:.2e}, worst out error / tolerance {worst:.3f}")
 
 
