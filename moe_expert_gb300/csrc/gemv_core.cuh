@@ -69,10 +69,12 @@ struct ActRegs {
 // Loads activations of block b (natural order: column c's quants at
 // xcol[c], its d scales at dcol[c][b * dstride]; dcol == nullptr gives unit
 // scales) into registers.  Invalid blocks get zeros.  The pointers may be
-// shared or global memory.
+// shared or global memory.  With `swap` (Q8_0 only) the two 16-byte halves
+// of the block are held in swapped order, to match a weight block read with
+// the same swap (the integer dot is the same sum in another order).
 template <int FMT, int C>
 __device__ __forceinline__ void load_act(ActRegs<FMT, C>& r, const int8_t* const* xcol, const float* const* dcol,
-                                         int b, bool valid, int li, int dstride = 1) {
+                                         int b, bool valid, int li, int dstride = 1, bool swap = false) {
 #pragma unroll
   for (int c = 0; c < C; ++c) {
     if (!valid) {
@@ -85,6 +87,11 @@ __device__ __forceinline__ void load_act(ActRegs<FMT, C>& r, const int8_t* const
     uint4 lo = *reinterpret_cast<const uint4*>(src);
     uint4 hi = *reinterpret_cast<const uint4*>(src + 16);
     if constexpr (FMT == MOEX_Q8_0) {
+      if (swap) {
+        const uint4 t = lo;
+        lo = hi;
+        hi = t;
+      }
       r.a[c][0] = lo.x; r.a[c][1] = lo.y; r.a[c][2] = lo.z; r.a[c][3] = lo.w;
       r.a[c][4] = hi.x; r.a[c][5] = hi.y; r.a[c][6] = hi.z; r.a[c][7] = hi.w;
     } else {
@@ -131,13 +138,27 @@ __device__ __forceinline__ void block_dots_from(uint4 q0, uint4 q1, float dw, co
   }
 }
 
-// Same, reading the block from memory at wq.
+// Same, reading the block from memory at wq; with `swap` (Q8_0) the second
+// 16-byte half first, for activations loaded with the same swap.
 template <int FMT, int C>
 __device__ __forceinline__ void block_row_dots(const uint8_t* wq, float dw, const ActRegs<FMT, C>& act, float* p,
-                                               int* I_out = nullptr) {
-  const uint4 q0 = *reinterpret_cast<const uint4*>(wq);
-  const uint4 q1 = FMT == MOEX_Q8_0 ? *reinterpret_cast<const uint4*>(wq + 16) : q0;
+                                               int* I_out = nullptr, bool swap = false) {
+  const int o0 = swap ? 16 : 0;
+  const uint4 q0 = *reinterpret_cast<const uint4*>(wq + o0);
+  const uint4 q1 = FMT == MOEX_Q8_0 ? *reinterpret_cast<const uint4*>(wq + (16 - o0)) : q0;
   block_dots_from<FMT, C>(q0, q1, dw, act, p, I_out);
+}
+
+// Shared-memory reads of Q8_0 blocks: lane li of a half warp reads its
+// 32-byte block at byte 32 * li of the row, so lanes li and li + 4 hit the
+// same four banks.  Lanes with bit 2 set read the second half first; then
+// lanes 0..7 cover all 32 banks and a half warp's 16-byte read takes two
+// wavefronts instead of four (it costs a per-lane address, so it is used
+// where shared-memory reads, not issue slots, bound the kernel).  Callers
+// load their activations with the same swap.
+template <int FMT>
+__device__ __forceinline__ bool smem_half_swap(int li) {
+  return FMT == MOEX_Q8_0 && ((li >> 2) & 1);
 }
 
 // ----------------------------------------------------------------- reduction
@@ -167,6 +188,42 @@ __device__ __forceinline__ void halving_reduce(float* v, int lane) {
 }
 
 __host__ __device__ constexpr int pow2_ceil(int v) { return v <= 1 ? 1 : 2 * pow2_ceil((v + 1) / 2); }
+
+// The same sums without the two selects per exchanged pair.  Each lane keeps
+// its values in the "xor layout": slot s holds logical value
+// s ^ xor_layout_mask<N>(lane), i.e. lanes with bit 3 set hold the two
+// halves swapped, lanes with bit 2 set the quarters inside them, and so on.
+// Then at every level a lane sends slot i + N/2 and keeps slot i, and the
+// pairs added are exactly those of halving_reduce, so both give the same
+// bits and leave the results in the same lanes.
+template <int N>
+__device__ __forceinline__ int xor_layout_mask(int lane) {
+  int m = 0;
+  if constexpr (N >= 2) m |= ((lane >> 3) & 1) * (N / 2);
+  if constexpr (N >= 4) m |= ((lane >> 2) & 1) * (N / 4);
+  if constexpr (N >= 8) m |= ((lane >> 1) & 1) * (N / 8);
+  if constexpr (N >= 16) m |= (lane & 1) * (N / 16);
+  return m;
+}
+
+template <int N, int O>
+__device__ __forceinline__ void halving_reduce_xl(float* v) {
+  if constexpr (O > 0) {
+    if constexpr (N > 1) {
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) v[i] = v[i] + __shfl_xor_sync(0xffffffffu, v[i + N / 2], O);
+      halving_reduce_xl<N / 2, O / 2>(v);
+    } else {
+      v[0] = v[0] + __shfl_xor_sync(0xffffffffu, v[0], O);
+      halving_reduce_xl<1, O / 2>(v);
+    }
+  }
+}
+
+// True when C values a lane can use the xor layout without padding slots:
+// C is a power of two, so slot c holds column c ^ xor_layout_mask<C>(lane).
+template <int C>
+__host__ __device__ constexpr bool xor_layout_ok() { return (C & (C - 1)) == 0; }
 
 // ----------------------------------------------------------------- consumer layout
 
@@ -276,7 +333,9 @@ __device__ __forceinline__ bool tma_ring_fill(const TmaRing& R, int it, const ui
 // Consumer side: per-lane partial sums of 8 rows (rows row0 .. row0+nrows-1
 // of the slot of ring stage `it`), after waiting for the slot to land when
 // `wait` is set.  Returns false on timeout / abort.
-template <int FMT, int C, int WPS, int N>
+// With SWAP, Q8_0 blocks are read with smem_half_swap and act must have been
+// loaded with the same swap.
+template <int FMT, int C, int WPS, int N, bool SWAP = false>
 __device__ __forceinline__ bool tma_ring_partials(const TmaRing& R, int it, const ConsumerPos& p, int nrows, int NB,
                                                   const ActRegs<FMT, C>& act, float (&v)[N], volatile int* abort,
                                                   int row0 = 0, bool wait = true) {
@@ -288,13 +347,14 @@ __device__ __forceinline__ bool tma_ring_partials(const TmaRing& R, int it, cons
   const int b = p.ks * SLICE + p.li;
   if (b >= NB) return true;
   constexpr int RPH = SR / (2 * WPS);
+  const bool swap = SWAP && smem_half_swap<FMT>(p.li);
 #pragma unroll
   for (int rr = 0; rr < RPH; ++rr) {
     const int row = p.jw * 2 + p.hf + 2 * WPS * rr;
     if (row < nrows) {
       const uint8_t* wq = st + row * R.qrow + b * FmtTraits<FMT>::QBYTES;
       const float dw = __half2float(reinterpret_cast<const __half*>(sc + row * R.scrow)[b]);
-      block_row_dots<FMT, C>(wq, dw, act, &v[rr * C]);
+      block_row_dots<FMT, C>(wq, dw, act, &v[rr * C], nullptr, swap);
     }
   }
   return true;

@@ -225,7 +225,7 @@ __device__ __forceinline__ void gu_unit(const DecodeArgs& a, const Groups& G, in
       dcol[c] = xd + t * S.NB;
     }
     const int b = pos.ks * SLICE + pos.li;
-    load_act<MOEX_Q8_0, C>(act, xcol, dcol, b, b < S.NB, pos.li);
+    load_act<MOEX_Q8_0, C>(act, xcol, dcol, b, b < S.NB, pos.li, 1, smem_half_swap<MOEX_Q8_0>(pos.li));
   }
   constexpr int N = Vals<C, WPS>::N;
   float* ub = ubuf + (ui % NUB) * 64 * S.NS * MAX_GROUP;
@@ -236,7 +236,7 @@ __device__ __forceinline__ void gu_unit(const DecodeArgs& a, const Groups& G, in
   for (int s = 0; s < 8; ++s) {
     const int it = ui * 8 + s;
     float v[N];
-    if (!tma_ring_partials<MOEX_Q8_0, C, WPS, N>(S.R, it, pos, SR, S.NB, act, v, S.abort_flag)) {
+    if (!tma_ring_partials<MOEX_Q8_0, C, WPS, N, true>(S.R, it, pos, SR, S.NB, act, v, S.abort_flag)) {
       ctx_abort(S, pos.lane, dead);
       return;
     }
@@ -437,7 +437,7 @@ __device__ __forceinline__ void dn_group(const DecodeArgs& a, const Groups& G, i
       dcol[c] = hd + j * S.NB;
     }
     const int b = pos.ks * SLICE + pos.li;
-    load_act<FMT, C>(act, xcol, dcol, b, b < S.NB, pos.li);
+    load_act<FMT, C>(act, xcol, dcol, b, b < S.NB, pos.li, 1, smem_half_swap<FMT>(pos.li));
   }
   constexpr int N = Vals<C, WPS>::N;
   const int gbase = G.gstart[g];
@@ -445,7 +445,7 @@ __device__ __forceinline__ void dn_group(const DecodeArgs& a, const Groups& G, i
   for (int rlo = 0; rlo < nrows; rlo += SR) {
     const int n = nrows - rlo < SR ? nrows - rlo : SR;
     float v[N];
-    if (!tma_ring_partials<FMT, C, WPS, N>(S.R, it0, pos, n, S.NB, act, v, S.abort_flag, rlo, rlo == 0)) {
+    if (!tma_ring_partials<FMT, C, WPS, N, true>(S.R, it0, pos, n, S.NB, act, v, S.abort_flag, rlo, rlo == 0)) {
       ctx_abort(S, pos.lane, dead);
       return;
     }

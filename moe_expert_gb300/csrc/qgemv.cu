@@ -236,18 +236,20 @@ __global__ void __launch_bounds__(640, MINB) qgemv_reg_kernel(GemvArgs a) {
     if (st < NSTG) load_stage(st, st);
   pdl_launch_dependents();
   pdl_wait();  // activations come from the previous kernel
+  constexpr int N = pow2_ceil(C);
+  constexpr bool XL = xor_layout_ok<C>();  // partial sums in the xor layout (select-free reduce)
+  const int cmask = XL ? xor_layout_mask<N>(lane) : 0;
   ActRegs<FMT, C> act;
   {
     const int8_t* xcol[C];
     const float* dcol[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) {
-      xcol[c] = a.xq + static_cast<int64_t>(c) * a.K;
-      dcol[c] = a.xds + static_cast<int64_t>(c) * a.NB * 2;
+      xcol[c] = a.xq + static_cast<int64_t>(c ^ cmask) * a.K;
+      dcol[c] = a.xds + static_cast<int64_t>(c ^ cmask) * a.NB * 2;
     }
     load_act<FMT, C>(act, xcol, dcol, b, bvalid, pos.li, 2);
   }
-  constexpr int N = pow2_ceil(C);
 #pragma unroll
   for (int st = 0; st < NSTG; ++st) {
     const int slot = st % P;
@@ -260,7 +262,10 @@ __global__ void __launch_bounds__(640, MINB) qgemv_reg_kernel(GemvArgs a) {
       block_dots_from<FMT, C>(q[slot][0], q[slot][QB16 - 1], __half2float(__ushort_as_half(hb)), act, v);
     }
     if (st + P < NSTG) load_stage(st + P, slot);  // refill the slot just consumed
-    halving_reduce<N, 8>(v, lane);
+    if constexpr (XL)
+      halving_reduce_xl<N, 8>(v);
+    else
+      halving_reduce<N, 8>(v, lane);
     // lane li holds value li / (16/N) (N < 16 always here)
     constexpr int REP = 16 / N;
     if (pos.li % REP == 0) {
