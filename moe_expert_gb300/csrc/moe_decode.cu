@@ -67,8 +67,9 @@ struct Groups {
 // Builds the groups from a shared-memory copy of the ids with every thread
 // of the block (n <= 64): entry j's position in (expert, entry) order is the
 // number of entries before it in that order; a group starts where the expert
-// changes or every MAX_GROUP entries of one expert.  Must be called by all
-// threads; ends with __syncthreads().
+// changes or every MAX_GROUP entries of one expert.  The starts are then
+// numbered by one warp with ballots over the 64 positions.  Must be called
+// by all threads (at least 64); ends with __syncthreads().
 __device__ void build_groups(Groups& G, const int32_t* ids, int n, int E, uint32_t* status, int* scratch) {
   // scratch: [MAX_ENTRIES] valid-position map
   const int j = threadIdx.x;
@@ -91,24 +92,33 @@ __device__ void build_groups(Groups& G, const int32_t* ids, int n, int E, uint32
     }
     G.ent[pos] = j;
   }
-  // group starts, by position
-  if (j < MAX_ENTRIES) scratch[j] = 0;
+  // by position: the expert of a group starting there, -2 for another
+  // valid entry, -1 past the valid entries
+  if (j < MAX_ENTRIES) scratch[j] = -1;
   __syncthreads();
-  if (e >= 0) scratch[pos] = ((pos - run) % MAX_GROUP == 0) ? 1 : 2;
+  if (e >= 0) scratch[pos] = ((pos - run) % MAX_GROUP == 0) ? e : -2;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int ng = 0, m = 0;
-    for (int p = 0; p < n; ++p) {
-      if (scratch[p] == 0) break;
-      if (scratch[p] == 1) {
-        G.gexp[ng] = ids[G.ent[p]];
-        G.gstart[ng] = p;
-        ++ng;
-      }
-      ++m;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int s0 = scratch[lane], s1 = scratch[lane + 32];
+    const unsigned st0 = __ballot_sync(0xffffffffu, s0 >= 0), st1 = __ballot_sync(0xffffffffu, s1 >= 0);
+    const unsigned v0 = __ballot_sync(0xffffffffu, s0 != -1), v1 = __ballot_sync(0xffffffffu, s1 != -1);
+    const unsigned below = (1u << lane) - 1u;
+    if (s0 >= 0) {
+      const int g = __popc(st0 & below);
+      G.gexp[g] = s0;
+      G.gstart[g] = lane;
     }
-    G.gstart[ng] = m;
-    G.ng = ng;
+    if (s1 >= 0) {
+      const int g = __popc(st0) + __popc(st1 & below);
+      G.gexp[g] = s1;
+      G.gstart[g] = lane + 32;
+    }
+    if (lane == 0) {
+      const int ng = __popc(st0) + __popc(st1);
+      G.gstart[ng] = __popc(v0) + __popc(v1);
+      G.ng = ng;
+    }
   }
   __syncthreads();
 }
@@ -425,14 +435,14 @@ __device__ __forceinline__ int dn_nstages(int nrows) { return (nrows + SR - 1) /
 template <int FMT, int C, int WPS>
 __device__ __forceinline__ void dn_group(const DecodeArgs& a, const Groups& G, int g, int it0, int nrows,
                                          const StageCtx& S, const ConsumerPos& pos, const int8_t* hs, const float* hd,
-                                         float* dred, int rows_max, bool& dead) {
+                                         float* dred, int rows_max, bool& dead, int c0 = 0, bool release = true) {
   ActRegs<FMT, C> act;
   {
     const int8_t* xcol[C];
     const float* dcol[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) {
-      const int j = G.ent[G.gstart[g] + c];
+      const int j = G.ent[G.gstart[g] + c0 + c];
       xcol[c] = hs + j * a.I;
       dcol[c] = hd + j * S.NB;
     }
@@ -440,7 +450,7 @@ __device__ __forceinline__ void dn_group(const DecodeArgs& a, const Groups& G, i
     load_act<FMT, C>(act, xcol, dcol, b, b < S.NB, pos.li, 1, smem_half_swap<FMT>(pos.li));
   }
   constexpr int N = Vals<C, WPS>::N;
-  const int gbase = G.gstart[g];
+  const int gbase = G.gstart[g] + c0;
   // the group's rows arrive as one ring slot; computed 8 rows at a time
   for (int rlo = 0; rlo < nrows; rlo += SR) {
     const int n = nrows - rlo < SR ? nrows - rlo : SR;
@@ -453,13 +463,15 @@ __device__ __forceinline__ void dn_group(const DecodeArgs& a, const Groups& G, i
       dred[(G.ent[gbase + c] * rows_max + rlo + row) * S.NS + pos.ks] = val;
     });
   }
-  tma_ring_release(S.R, it0, pos.lane);
+  if (release) tma_ring_release(S.R, it0, pos.lane);
 }
 
 // TEAMS teams of NS consumer warps (one warp per K slice) take the groups
 // round robin, so several groups are in flight at once: a group is little
 // work behind a long chain of waits, loads and reductions.
-template <int FMT, int TEAMS, int MAXT>
+// CMAX == 2: groups are taken two entries at a time, which keeps the kernel
+// small enough in registers for ten teams.
+template <int FMT, int TEAMS, int MAXT, int CMAX = MAX_GROUP>
 __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   MOEX_TRACE_BEGIN();
@@ -551,18 +563,29 @@ __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
   bool dead = false;
   for (int g = team; g < G.ng && !dead; g += TEAMS) {
     const int m = G.gstart[g + 1] - G.gstart[g];
+    if constexpr (CMAX == 2) {
+      // entries two at a time (the slot is read again; each entry's dot
+      // products are the same bits for any number of columns)
+      for (int c0 = 0; c0 < m && !dead; c0 += 2) {
+        if (m - c0 >= 2)
+          dn_group<FMT, 2, 1>(a, G, g, g, nrows, S, pos, hs, hd, osum, rows_max, dead, c0, c0 + 2 >= m);
+        else
+          dn_group<FMT, 1, 1>(a, G, g, g, nrows, S, pos, hs, hd, osum, rows_max, dead, c0, true);
+      }
+    } else {
 #define MOEX_DN(CC) dn_group<FMT, CC, 1>(a, G, g, g, nrows, S, pos, hs, hd, osum, rows_max, dead)
-    switch (m) {
-      case 1: MOEX_DN(1); break;
-      case 2: MOEX_DN(2); break;
-      case 3: MOEX_DN(3); break;
-      case 4: MOEX_DN(4); break;
-      case 5: MOEX_DN(5); break;
-      case 6: MOEX_DN(6); break;
-      case 7: MOEX_DN(7); break;
-      default: MOEX_DN(8); break;
-    }
+      switch (m) {
+        case 1: MOEX_DN(1); break;
+        case 2: MOEX_DN(2); break;
+        case 3: MOEX_DN(3); break;
+        case 4: MOEX_DN(4); break;
+        case 5: MOEX_DN(5); break;
+        case 6: MOEX_DN(6); break;
+        case 7: MOEX_DN(7); break;
+        default: MOEX_DN(8); break;
+      }
 #undef MOEX_DN
+    }
     if (g == team) MOEX_TRACE_STAMP(2);
   }
   MOEX_TRACE_STAMP(3);
@@ -618,7 +641,7 @@ moex_status launch_gu(const DecodeArgs& base, int smem_cap, cudaStream_t s) {
   return cuda_status(launch_pdl(kern, dim3(grid), dim3(threads), L.total, s, a));
 }
 
-template <int FMT, int TEAMS, int MAXT>
+template <int FMT, int TEAMS, int MAXT, int CMAX = MAX_GROUP>
 moex_status launch_dn(const DecodeArgs& base, int smem_cap, cudaStream_t s) {
   DecodeArgs a = base;
   const int NB = a.I / QK, NS = num_slices(NB);
@@ -632,7 +655,7 @@ moex_status launch_dn(const DecodeArgs& base, int smem_cap, cudaStream_t s) {
   if (nst < 2) return MOEX_EUNSUPPORTED;
   a.nst = nst;
   const DnSmem L(a.n, a.I, NS, rows_max, nst, slot_bytes);
-  auto kern = moe_dn_kernel<FMT, TEAMS, MAXT>;
+  auto kern = moe_dn_kernel<FMT, TEAMS, MAXT, CMAX>;
   if (ensure_smem(reinterpret_cast<const void*>(kern), L.total) != cudaSuccess) return MOEX_ECUDA;
   const int threads = (NS * TEAMS + 1) * 32;
   return cuda_status(launch_pdl(kern, dim3(grid), dim3(threads), L.total, s, a));
@@ -645,7 +668,7 @@ template <int FMT>
 moex_status launch_dn_fmt(const DecodeArgs& a, int cap, cudaStream_t s) {
   const int NS = num_slices(a.I / QK);
   const int wps = decode_wps(NS);
-  if (wps == 4) return launch_dn<FMT, 5, 512>(a, cap, s);  // five teams of up to three slice warps
+  if (wps == 4) return launch_dn<FMT, 10, 992, 2>(a, cap, s);  // ten teams of up to three slice warps
   if (wps == 2) return (NS * 2 + 1) * 32 <= 352 ? launch_dn<FMT, 2, 352>(a, cap, s) : launch_dn<FMT, 2, 544>(a, cap, s);
   return (NS + 1) * 32 <= 352 ? launch_dn<FMT, 1, 352>(a, cap, s) : launch_dn<FMT, 1, 544>(a, cap, s);
 }
