@@ -405,9 +405,9 @@ __global__ void __launch_bounds__(MAXT, 1) moe_gu_kernel(DecodeArgs a) {
 // ============================================================== down + combine
 
 struct DnSmem {
-  int bars, cnt, abort_flag, ids, groups, hs, hd, red, osum, ring, total;
+  int bars, cnt, abort_flag, ids, groups, red, osum, ring, total;
   __host__ __device__ DnSmem(int n, int I, int NS, int rows_max, int nst, int slot_bytes) {
-    const int NB = I / QK;
+    (void)I;
     int o = 0;
     bars = o; o += 16 * nst;
     cnt = o; o += 4 * nst;
@@ -415,10 +415,6 @@ struct DnSmem {
     ids = o; o += 8 * MAX_ENTRIES;
     o = (o + 15) & ~15;
     groups = o; o += static_cast<int>(sizeof(Groups));
-    o = (o + 15) & ~15;
-    hs = o; o += n * I;
-    o = (o + 15) & ~15;
-    hd = o; o += 4 * n * NB;
     o = (o + 15) & ~15;
     red = o; o += 4 * n * rows_max * NS;   // [entry][row][ks]
     osum = red;
@@ -434,7 +430,7 @@ __device__ __forceinline__ int dn_nstages(int nrows) { return (nrows + SR - 1) /
 
 template <int FMT, int C, int WPS>
 __device__ __forceinline__ void dn_group(const DecodeArgs& a, const Groups& G, int g, int it0, int nrows,
-                                         const StageCtx& S, const ConsumerPos& pos, const int8_t* hs, const float* hd,
+                                         const StageCtx& S, const ConsumerPos& pos,
                                          float* dred, int rows_max, bool& dead, int c0 = 0, bool release = true) {
   ActRegs<FMT, C> act;
   {
@@ -443,11 +439,11 @@ __device__ __forceinline__ void dn_group(const DecodeArgs& a, const Groups& G, i
 #pragma unroll
     for (int c = 0; c < C; ++c) {
       const int j = G.ent[G.gstart[g] + c0 + c];
-      xcol[c] = hs + j * a.I;
-      dcol[c] = hd + j * S.NB;
+      xcol[c] = a.hq + static_cast<int64_t>(j) * a.I;
+      dcol[c] = a.hds + static_cast<int64_t>(j) * S.NB * 2;
     }
     const int b = pos.ks * SLICE + pos.li;
-    load_act<FMT, C>(act, xcol, dcol, b, b < S.NB, pos.li, 1, smem_half_swap<FMT>(pos.li));
+    load_act<FMT, C>(act, xcol, dcol, b, b < S.NB, pos.li, 2, smem_half_swap<FMT>(pos.li));
   }
   constexpr int N = Vals<C, WPS>::N;
   const int gbase = G.gstart[g] + c0;
@@ -499,8 +495,6 @@ __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
   S.status = a.status;
   int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L.ids);
   Groups& G = *reinterpret_cast<Groups*>(smem + L.groups);
-  int8_t* hs = reinterpret_cast<int8_t*>(smem + L.hs);
-  float* hd = reinterpret_cast<float*>(smem + L.hd);
   float* osum = reinterpret_cast<float*>(smem + L.osum);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -545,19 +539,13 @@ __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
     return;
   }
 
-  // consumers: Hq of every entry into shared memory, after the gate/up grid
+  // consumers: each team reads its entries' Hq blocks straight from global
+  // memory into registers, after the gate/up grid
   pdl_wait();
   MOEX_TRACE_STAMP(1);
   const int nthr = nwc * 32;
-  {
-    const int4* src = reinterpret_cast<const int4*>(a.hq);
-    int4* dst = reinterpret_cast<int4*>(hs);
-    for (int i = threadIdx.x; i < a.n * a.I / 16; i += nthr) dst[i] = src[i];
-    const float2* dsrc = reinterpret_cast<const float2*>(a.hds);
-    for (int i = threadIdx.x; i < a.n * NB; i += nthr) hd[i] = dsrc[i].x;
-    for (int i = threadIdx.x; i < a.n * rows_max * NS; i += nthr) osum[i] = 0.f;
-    named_bar_sync(1, nthr);
-  }
+  for (int i = threadIdx.x; i < a.n * rows_max * NS; i += nthr) osum[i] = 0.f;
+  named_bar_sync(1, nthr);
   const int team = warp / NS;
   const ConsumerPos pos = consumer_pos(warp % NS, lane, 1);
   bool dead = false;
@@ -568,12 +556,12 @@ __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
       // products are the same bits for any number of columns)
       for (int c0 = 0; c0 < m && !dead; c0 += 2) {
         if (m - c0 >= 2)
-          dn_group<FMT, 2, 1>(a, G, g, g, nrows, S, pos, hs, hd, osum, rows_max, dead, c0, c0 + 2 >= m);
+          dn_group<FMT, 2, 1>(a, G, g, g, nrows, S, pos, osum, rows_max, dead, c0, c0 + 2 >= m);
         else
-          dn_group<FMT, 1, 1>(a, G, g, g, nrows, S, pos, hs, hd, osum, rows_max, dead, c0, true);
+          dn_group<FMT, 1, 1>(a, G, g, g, nrows, S, pos, osum, rows_max, dead, c0, true);
       }
     } else {
-#define MOEX_DN(CC) dn_group<FMT, CC, 1>(a, G, g, g, nrows, S, pos, hs, hd, osum, rows_max, dead)
+#define MOEX_DN(CC) dn_group<FMT, CC, 1>(a, G, g, g, nrows, S, pos, osum, rows_max, dead)
       switch (m) {
         case 1: MOEX_DN(1); break;
         case 2: MOEX_DN(2); break;
