@@ -100,10 +100,21 @@ def _torch():
     return torch
 
 
+_raw_stream = None
+
+
 def _stream(stream=None) -> ctypes.c_void_p:
+    """The handle of `stream`, else of torch's current stream on the current
+    device (read without building a Stream object when torch offers that)."""
+    global _raw_stream
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
     torch = _torch()
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if _raw_stream is None:
+        _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None) or False
+    if _raw_stream:
+        return ctypes.c_void_p(_raw_stream(torch.cuda.current_device()))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def _ptr(t) -> ctypes.c_void_p:
