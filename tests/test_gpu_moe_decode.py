@@ -91,6 +91,17 @@ def test_decode_small(T, k, E, hidden, inter, dn_fmt):
     run_checks(E, hidden, inter, x, ids, w, dn_fmt=dn_fmt, seed=3)
 
 
+def test_decode_wide_layer():
+    """hidden 4096 and inter 2048: eight K slices in gate/up (one warp per
+    slice) and four in down (two-team down kernel), the variants the
+    2560 x 1536 workload does not reach."""
+    T, k, E, hidden, inter = 2, 4, 8, 4096, 2048
+    g = synth.rng(77)
+    x = synth.activations(g, T, hidden)
+    ids, w = om.route_topk(synth.router_logits(g, T, E), k)
+    run_checks(E, hidden, inter, x, ids, w, seed=5)
+
+
 def test_decode_repeated_expert_and_single_expert_chain():
     """All 8 slots on one expert (more entries than a group pass holds when
     T = 2) equals the single-expert chain."""
