@@ -101,3 +101,70 @@ def test_decode_validation_and_workspace():
     assert L.moex_moe_decode(ctypes.byref(gu), ctypes.byref(dn_bad), p, 3, p, p, 8, p, p, 1 << 30, null) == 1
     gu_iq = mx.QWeight(2, 128, 3072, 2560, base, base)                     # gate/up must be Q8_0
     assert L.moex_moe_decode(ctypes.byref(gu_iq), ctypes.byref(dn), p, 3, p, p, 8, p, p, 1 << 30, null) == 3
+
+
+def test_prefill_and_dense_validation():
+    """The prefill entry points reject bad arguments on the host, in the
+    order their checks run, before anything is enqueued."""
+    import moe_expert_gb300 as mx
+    L = ensure_lib()
+    null = ctypes.c_void_p(0)
+    buf = ctypes.create_string_buffer(4096 + 16)
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    p = ctypes.c_void_p(base)
+    odd = ctypes.c_void_p(base + 4)
+    E, H, I, T, k = 4, 256, 128, 8, 2
+    gu = mx.QWeight(2, E, 2 * I, H, base, base)
+    dn = mx.QWeight(2, E, H, I, base, base)
+    need = L.moex_moe_prefill_workspace_bytes(T, k, E, H, I)
+    assert need > 0
+    assert L.moex_moe_prefill_workspace_bytes(0, k, E, H, I) == 0
+    big = 1 << 40
+
+    def pf(g=gu, d=dn, x=p, t=T, kk=k, out=p, ws=p, nbytes=big):
+        return L.moex_moe_prefill(ctypes.byref(g), ctypes.byref(d), x, t, p, p, kk, out, ws, nbytes, null)
+
+    assert pf(x=null) == 1
+    assert pf(t=0) == 1
+    assert pf(kk=17) == 1
+    assert pf(d=mx.QWeight(2, E + 1, H, I, base, base)) == 1            # expert counts differ
+    assert pf(d=mx.QWeight(2, E, H, 2 * I, base, base)) == 1            # down K != inter
+    assert pf(g=mx.QWeight(2, E, 2 * I, 96, base, base),
+              d=mx.QWeight(2, E, 96, I, base, base)) == 3               # hidden not a multiple of 128
+    assert pf(nbytes=need - 1) == 7
+    assert pf(x=odd) == 2
+    assert pf(out=odd) == 2
+    assert L.moex_moe_prefill_residual(ctypes.byref(gu), ctypes.byref(dn), p, T, p, p, k, null, p, p, big,
+                                       null) == 1
+    assert L.moex_moe_prefill_residual(ctypes.byref(gu), ctypes.byref(dn), p, T, p, p, k, odd, p, p, big,
+                                       null) == 2
+
+    W = mx.QWeight(2, 1, 256, 128, base, base)
+    dneed = L.moex_dense_prefill_workspace_bytes(T, 256, 128)
+    assert dneed > 0 and L.moex_dense_prefill_workspace_bytes(T, 64, 128) == 0
+
+    def dp(w=W, x=p, y=p, ldy=256, ws=p, nbytes=big):
+        return L.moex_dense_prefill(ctypes.byref(w), x, T, y, ldy, ws, nbytes, null)
+
+    assert dp(w=mx.QWeight(2, 2, 256, 128, base, base)) == 3          # one matrix only
+    assert dp(y=null) == 1
+    assert dp(ldy=255) == 1
+    assert dp(w=mx.QWeight(2, 1, 192, 128, base, base), ldy=192) == 3  # rows not a multiple of 128
+    assert dp(w=mx.QWeight(2, 1, 256, 96, base, base)) == 3           # K not a multiple of 64
+    assert dp(nbytes=dneed - 1) == 7
+    assert dp(x=odd) == 2
+
+
+def test_decode_residual_validation():
+    import moe_expert_gb300 as mx
+    L = ensure_lib()
+    null = ctypes.c_void_p(0)
+    buf = ctypes.create_string_buffer(4096 + 16)
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    p = ctypes.c_void_p(base)
+    gu = mx.QWeight(1, 16, 512, 256, base, base)
+    dn = mx.QWeight(2, 16, 256, 256, base, base)
+    big = 1 << 30
+    assert L.moex_moe_decode_residual(ctypes.byref(gu), ctypes.byref(dn), p, 2, p, p, 4, null, p, p, big, null) == 1
+    assert L.moex_moe_decode_residual(ctypes.byref(gu), ctypes.byref(dn), p, 2, p, p, 4, ctypes.c_void_p(base + 8),
+                                      p, p, big, null) == 2
