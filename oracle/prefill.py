@@ -32,8 +32,10 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 
 
 def fp16_rn(x: np.ndarray) -> np.ndarray:
-    """Round to FP16, nearest even, straight from the given precision."""
-    return np.asarray(x).astype(np.float16)
+    """Round to FP16, nearest even, straight from the given precision.
+    Magnitudes past the FP16 range become inf, as IEEE rounding gives."""
+    with np.errstate(over="ignore"):
+        return np.asarray(x).astype(np.float16)
 
 
 def dequant_fp16(fmt: str, blocks: np.ndarray) -> np.ndarray:
