@@ -140,6 +140,23 @@ moex_status moex_qgemv_block_dots(const moex_qweight* W, const int8_t* xq, int n
                                   moex_stream stream);
 
 /*
+ * Test hook for the failure path of the bounded device waits (no counterpart
+ * on the pages: they describe no failure detection).  Launches the
+ * shared-memory-ring variant of the one-column moex_qgemv kernel with its
+ * copy producer switched off: it issues no copy at all, so every consumer
+ * warp's wait for its first weight stage runs out after wait_limit_ns
+ * nanoseconds of %globaltimer, sets the "copy-pipeline wait ran out" bit of
+ * the device status word and returns.  No copy is in flight when the kernel
+ * exits, the context stays usable, and y is left undefined.
+ *   Arguments as moex_qgemv with ncols == 1 and K <= 2560;
+ *   1e5 <= wait_limit_ns <= 2e9.
+ * Afterwards moex_device_status() returns MOEX_ETIMEOUT (and clears the
+ * word); the next regular call runs normally.
+ */
+moex_status moex_debug_qgemv_starved(const moex_qweight* W, const int8_t* xq, const float* xds, int ncols, float* y,
+                                     int64_t ldy, uint64_t wait_limit_ns, moex_stream stream);
+
+/*
  * Router: top-k experts of each token's logits (descending logit, ties to the
  * lower expert id) and the softmax over the k selected logits (max
  * subtracted; FP32 expf).
@@ -279,7 +296,10 @@ moex_status moex_moe_prefill_residual(const moex_qweight* gate_up, const moex_qw
  *   byte it reads).  Calls that may overlap on the GPU -- on different
  *   streams, or from several threads -- race on the buffer and must be
  *   serialised by the caller.
- * Arguments and results are those of moex_moe_decode.
+ * Arguments and results are those of moex_moe_decode, and so are the
+ * argument checks, in the same order: a malformed call returns the status
+ * moex_moe_decode would return, and MOEX_ENOSPACE means only that a
+ * well-formed layer needs more than the built-in buffer.
  */
 moex_status moex_moe_decode_noalloc(const moex_qweight* gate_up, const moex_qweight* down, const float* x, int T,
                                     const int32_t* ids, const float* w, int k, float* out, moex_stream stream);

@@ -53,6 +53,7 @@ SIGNATURES = {
     "moex_quantize_q8_1": (ctypes.c_int, [_P, _I64, ctypes.c_int, _I64, _P, _P, _P]),
     "moex_qgemv": (ctypes.c_int, [_QWP, _P, _P, ctypes.c_int, _P, _I64, _P]),
     "moex_qgemv_block_dots": (ctypes.c_int, [_QWP, _P, ctypes.c_int, _P, _P]),
+    "moex_debug_qgemv_starved": (ctypes.c_int, [_QWP, _P, _P, ctypes.c_int, _P, _I64, ctypes.c_uint64, _P]),
     "moex_route_topk": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P]),
     "moex_moe_decode_workspace_bytes": (_SZ, [ctypes.c_int, ctypes.c_int, _I64, _I64]),
     "moex_moe_decode": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _SZ, _P]),

@@ -180,6 +180,18 @@ moex_status moex_qgemv_block_dots(const moex_qweight* W, const int8_t* xq, int n
   return launch_block_dots(W, xq, ncols, dots, stream);
 }
 
+moex_status moex_debug_qgemv_starved(const moex_qweight* W, const int8_t* xq, const float* xds, int ncols, float* y,
+                                     int64_t ldy, uint64_t wait_limit_ns, moex_stream stream) {
+  const moex_status st = check_weight(W);
+  if (st != MOEX_OK) return st;
+  if (W->n_mats != 1) return MOEX_EINVAL;
+  if (!xq || !xds || !y || ncols != 1 || ldy < W->rows) return MOEX_EINVAL;
+  if (W->rows > (int64_t(1) << 31)) return MOEX_EINVAL;
+  if (wait_limit_ns < 100000ull || wait_limit_ns > WAIT_LIMIT_NS) return MOEX_EINVAL;
+  if (!aligned16(xq) || !aligned8(xds)) return MOEX_EALIGN;
+  return launch_qgemv_starved(W, xq, xds, ncols, y, ldy, wait_limit_ns, stream);
+}
+
 moex_status moex_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, moex_stream stream) {
   if (!logits || !ids || !w) return MOEX_EINVAL;
   if (T < 1 || k < 1 || k > 16 || E < k || E > 1024) return MOEX_EINVAL;
@@ -191,7 +203,11 @@ size_t moex_moe_decode_workspace_bytes(int T, int k, int64_t hidden, int64_t int
   return moe_decode_ws_bytes(T, k, hidden, inter);
 }
 
-static moex_status check_decode(const moex_qweight* gate_up, const moex_qweight* down, const float* x, int T,
+}  // extern "C"
+
+namespace moex {
+
+moex_status check_decode(const moex_qweight* gate_up, const moex_qweight* down, const float* x, int T,
                                 const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes) {
   moex_status st = check_weight(gate_up);
   if (st != MOEX_OK) return st;
@@ -207,6 +223,10 @@ static moex_status check_decode(const moex_qweight* gate_up, const moex_qweight*
   if (!aligned16(x) || !aligned16(ws)) return MOEX_EALIGN;
   return MOEX_OK;
 }
+
+}  // namespace moex
+
+extern "C" {
 
 moex_status moex_moe_decode(const moex_qweight* gate_up, const moex_qweight* down, const float* x, int T,
                             const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,

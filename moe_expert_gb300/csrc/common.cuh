@@ -99,15 +99,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false if it
-// has not completed within WAIT_LIMIT_NS or if *abort becomes non-zero.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// has not completed within limit_ns (WAIT_LIMIT_NS unless a caller passes a
+// shorter limit) or if *abort becomes non-zero.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (abort && *abort) return false;
-      if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
 }

@@ -338,10 +338,11 @@ __device__ __forceinline__ bool tma_ring_fill(const TmaRing& R, int it, const ui
 template <int FMT, int C, int WPS, int N, bool SWAP = false>
 __device__ __forceinline__ bool tma_ring_partials(const TmaRing& R, int it, const ConsumerPos& p, int nrows, int NB,
                                                   const ActRegs<FMT, C>& act, float (&v)[N], volatile int* abort,
-                                                  int row0 = 0, bool wait = true) {
+                                                  int row0 = 0, bool wait = true,
+                                                  uint64_t limit_ns = WAIT_LIMIT_NS) {
 #pragma unroll
   for (int i = 0; i < N; ++i) v[i] = 0.f;
-  if (wait && !mbar_wait(&R.full[it % R.nst], (it / R.nst) & 1, abort)) return false;
+  if (wait && !mbar_wait(&R.full[it % R.nst], (it / R.nst) & 1, abort, limit_ns)) return false;
   const uint8_t* st = R.slot(it) + row0 * R.qrow;
   const uint8_t* sc = R.slot(it) + R.slot_rows * R.qrow + row0 * R.scrow;
   const int b = p.ks * SLICE + p.li;

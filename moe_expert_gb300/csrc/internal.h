@@ -46,12 +46,19 @@ moex_status launch_weight_pack(const moex_qweight* w, const void* blocks, cudaSt
 moex_status launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
 moex_status launch_qgemv(const moex_qweight* W, const int8_t* xq, const float* xds, int ncols, float* y,
                          int64_t ldy, cudaStream_t s);
+moex_status launch_qgemv_starved(const moex_qweight* W, const int8_t* xq, const float* xds, int ncols, float* y,
+                                 int64_t ldy, uint64_t wait_ns, cudaStream_t s);
 moex_status launch_block_dots(const moex_qweight* W, const int8_t* xq, int ncols, int32_t* dots, cudaStream_t s);
 size_t moe_decode_ws_bytes(int T, int k, int64_t hidden, int64_t inter);
 moex_status launch_moe_decode(const moex_qweight* gu, const moex_qweight* dn, const float* x, int T,
                               const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,
                               float* gu_dbg, float* h_dbg, int8_t* hq_dbg, float* hds_dbg, const float* residual,
                               cudaStream_t s);
+
+// Host checks of the decode layer's arguments (every check of
+// moex_moe_decode, in its order, the workspace size last but one).
+moex_status check_decode(const moex_qweight* gate_up, const moex_qweight* down, const float* x, int T,
+                         const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes);
 
 size_t moe_prefill_ws_bytes(int T, int k, int E, int64_t hidden, int64_t inter);
 void prefill_ws_layout(int T, int k, int E, int64_t hidden, int64_t inter, size_t* off);

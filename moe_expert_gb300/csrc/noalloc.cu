@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "../../include/moex.h"
+#include "internal.h"
 
 namespace {
 
@@ -48,12 +49,14 @@ extern "C" {
 
 moex_status moex_moe_decode_noalloc(const moex_qweight* gate_up, const moex_qweight* down, const float* x, int T,
                                     const int32_t* ids, const float* w, int k, float* out, moex_stream stream) {
-  if (!gate_up || !down) return MOEX_EINVAL;
-  const size_t need = moex_moe_decode_workspace_bytes(T, k, gate_up->K, down->K);
-  if (need == 0) return MOEX_EINVAL;
-  if (need > NOALLOC_SCRATCH_BYTES) return MOEX_ENOSPACE;  // the layer needs more than the built-in buffer
   void* scratch = scratch_address();
   if (!scratch) return MOEX_ECUDA;
+  // The checks of moex_moe_decode, in its order, with the built-in buffer as
+  // the workspace: a malformed call gets the same status it would get there,
+  // and a well-formed layer that needs more than the buffer gets
+  // MOEX_ENOSPACE.
+  const moex_status st = moex::check_decode(gate_up, down, x, T, ids, w, k, out, scratch, NOALLOC_SCRATCH_BYTES);
+  if (st != MOEX_OK) return st;
   // Nothing in the scratch has to start at zero: the gate/up kernel writes
   // every byte of it that the down kernel reads.
   return moex_moe_decode(gate_up, down, x, T, ids, w, k, out, scratch, NOALLOC_SCRATCH_BYTES, stream);

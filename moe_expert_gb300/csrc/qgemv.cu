@@ -23,6 +23,8 @@ struct GemvArgs {
   float* y;
   int64_t ldy;
   uint32_t* status;
+  uint64_t wait_ns;     // limit of every bounded wait (WAIT_LIMIT_NS)
+  int starve;           // test hook: the ring producer issues no copies
 };
 
 
@@ -111,7 +113,7 @@ __global__ void __launch_bounds__(GemvBounds<WPS, MINB, CS>::MAXT, MINB) qgemv_k
   pdl_launch_dependents();
 
   if (warp == nwc) {
-    if (lane == 0) {
+    if (lane == 0 && !a.starve) {
       const uint64_t pol = l2_evict_first_policy();
       int issued = 0;
       for (int it = 0; it < nstage; ++it) {
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(GemvBounds<WPS, MINB, CS>::MAXT, MINB) qgemv_k
     for (int it = c0; it < c1 && !dead; ++it) {
       const int n = stage_rows(it);
       float v[N];
-      if (!tma_ring_partials<FMT, CG, WPS, N>(R, it, pos, n, a.NB, act, v, abort_flag)) {
+      if (!tma_ring_partials<FMT, CG, WPS, N>(R, it, pos, n, a.NB, act, v, abort_flag, 0, true, a.wait_ns)) {
         if (lane == 0) {
           *abort_flag = 1;
           flag_status(a.status, DEV_TIMEOUT_PIPE);
@@ -400,6 +402,8 @@ moex_status launch_qgemv(const moex_qweight* W, const int8_t* xq, const float* x
   a.scrow = static_cast<int>(sc_row_bytes(W->K));
   a.stage_bytes = ((SR * (a.qrow + a.scrow)) + 127) & ~127;
   a.status = device_status_ptr();
+  a.wait_ns = WAIT_LIMIT_NS;
+  a.starve = 0;
   if (a.NS > 16) return MOEX_EUNSUPPORTED;
   const int cap = max_smem_optin();
   for (int c0 = 0; c0 < ncols; c0 += 8) {
@@ -413,6 +417,31 @@ moex_status launch_qgemv(const moex_qweight* W, const int8_t* xq, const float* x
     if (st != MOEX_OK) return st;
   }
   return MOEX_OK;
+}
+
+moex_status launch_qgemv_starved(const moex_qweight* W, const int8_t* xq, const float* xds, int ncols, float* y,
+                                 int64_t ldy, uint64_t wait_ns, cudaStream_t s) {
+  GemvArgs a = {};
+  a.qs = static_cast<const uint8_t*>(W->qs);
+  a.sc = static_cast<const uint8_t*>(W->scales);
+  a.rows = W->rows;
+  a.K = static_cast<int>(W->K);
+  a.NB = a.K / QK;
+  a.NS = num_slices(a.NB);
+  a.qrow = static_cast<int>(qs_row_bytes(W->fmt, W->K));
+  a.scrow = static_cast<int>(sc_row_bytes(W->K));
+  a.status = device_status_ptr();
+  a.wait_ns = wait_ns;
+  a.starve = 1;
+  a.xq = xq;
+  a.xds = xds;
+  a.y = y;
+  a.ldy = ldy;
+  if (a.NS > 5) return MOEX_EUNSUPPORTED;
+  // the ring variant of the one-column GEMV (the register-staged kernel has no producer)
+  const int cap = max_smem_optin();
+  (void)ncols;
+  return W->fmt == MOEX_Q8_0 ? launch_one<MOEX_Q8_0, 1, 2, 2>(a, cap, s) : launch_one<MOEX_IQ4_NL, 1, 2, 2>(a, cap, s);
 }
 
 moex_status launch_block_dots(const moex_qweight* W, const int8_t* xq, int ncols, int32_t* dots, cudaStream_t s) {

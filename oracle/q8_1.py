@@ -57,8 +57,3 @@ def quantize_q8_1(x: np.ndarray):
     d = np.where(nz, d, np.float32(0.0)).astype(np.float32)
     return q.reshape(C, K), d, s
 
-
-def dequantize_q8_1(q: np.ndarray, d: np.ndarray) -> np.ndarray:
-    """d * q per block, float64 [ncols, K] (exact)."""
-    C, K = q.shape
-    return (np.repeat(d.astype(np.float64), QK, axis=1) * q.astype(np.float64)).reshape(C, K)

@@ -24,9 +24,10 @@ def to_np(t):
 
 def assert_within(got, ref, A, what=""):
     """|got - ref| <= 1e-5 * A + 1e-6 elementwise (the GEMV pass rule)."""
+    from oracle.gemv import tolerance
     got = np.asarray(got, dtype=np.float64)
     err = np.abs(got - ref)
-    tol = 1e-5 * A + 1e-6
+    tol = tolerance(np.asarray(A, dtype=np.float64))
     bad = err > tol
     if bad.any():
         i = np.unravel_index(np.argmax(err - tol), err.shape)

@@ -220,6 +220,38 @@ def test_gemv_brute_force_tiny(fmt):
             assert abs(A[c, r] - float(absum)) <= 1e-12 * float(absum)
 
 
+def read_bound_case():
+    vals = {}
+    with open(os.path.join(GOLDEN, "gemv_bound_hand.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                key, val = line.split(":", 1)
+                vals[key.strip()] = [float(v) for v in val.split()]
+    return vals
+
+
+def test_gemv_error_scale_and_tolerance_hand_fixture():
+    """y, A and the pass bound of a two-block row worked out by hand
+    (tests/golden/gemv_bound_hand.txt)."""
+    c = read_bound_case()
+    wq = np.zeros((1, 64), dtype=np.int64)
+    xq = np.zeros((1, 64), dtype=np.int64)
+    for b in (0, 1):
+        for i, v in enumerate(c[f"qw{b}"]):
+            wq[0, 32 * b + i] = int(v)
+        for i, v in enumerate(c[f"qx{b}"]):
+            xq[0, 32 * b + i] = int(v)
+    dw = np.array([c["dw"]], dtype=np.float32)
+    dx = np.array([c["dx"]], dtype=np.float32)
+    y, A = gemv.gemv_planes(dw, wq, dx, xq)
+    assert y[0, 0] == c["y"][0]
+    assert A[0, 0] == c["A"][0]
+    assert abs(gemv.tolerance(A)[0, 0] - c["bound"][0]) < 1e-15
+    # the bound is exactly 1e-5 * A + 1e-6 element by element, monotone in A
+    a = np.array([0.0, 1.0, 1e5])
+    assert np.array_equal(gemv.tolerance(a), np.array([1e-6, 1e-5 + 1e-6, 1.0 + 1e-6]))
+
+
 def test_block_dots_brute_force_and_range():
     g = synth.rng(8)
     wq = g.integers(-127, 128, (3, 64))
