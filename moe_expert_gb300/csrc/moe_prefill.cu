@@ -13,19 +13,18 @@
 // with Wh = fp16_rn(fp32(d) * kvalues[idx]).
 //
 // GB300 design (not the pages' wmma kernels): the weights are the MMA's A
-// operand and live in tensor memory: four warps dequantise 128 weight rows x
-// 64 inputs per k-step straight from the IQ4_NL planes into TMEM with
-// tcgen05.st (one thread per row, no shared-memory round trip); the sorted
-// token rows are the B operand, 32-row boxes of a 2-D TMA tensor map with the
-// 128-byte swizzle; one thread issues tcgen05.mma (M = 128, N = tile tokens
-// rounded to 16, K = 16) into a double-buffered FP32 accumulator in TMEM, and
-// four epilogue warps read it back with tcgen05.ld.  Because the token count
-// of an expert is the MMA's N, ragged experts cost at most 15 padded columns
-// per tile instead of a partial 128-row M tile.  CTAs run in clusters of two
-// on the same token tile (neighbouring feature tiles): each loads half of the
-// token boxes with TMA multicast into both, since one SM's TMA unit cannot
-// feed an M = 128 MMA from L2 at full rate, and each CTA's MMA completion is
-// committed to the release barriers of both.
+// operand and live in tensor memory: eight warps dequantise 128 weight rows x
+// 64 inputs per k-step straight from the IQ4_NL (or Q8_0) planes into TMEM
+// with tcgen05.st (one thread per row, no shared-memory round trip); the
+// sorted token rows are the B operand, boxes of a 2-D TMA tensor map with the
+// 128-byte swizzle; tcgen05.mma (K = 16, N = tile tokens rounded up) into a
+// double-buffered FP32 accumulator in TMEM, read back by four epilogue warps
+// with tcgen05.ld.  Because the token count of an expert is the MMA's N,
+// ragged experts cost a few padded columns per tile instead of a partial
+// 128-row M tile.  CTAs run in pairs (clusters of two) on neighbouring
+// feature tiles of the same token tile and share M = 256 MMAs (tcgen05
+// cta_group::2): each CTA loads only its half of the token rows, so the
+// shared-memory traffic of the B operand per SM is halved.
 //
 // K order: every FP16 operand of the two GEMMs stores each 32-input block
 // interleaved (position 2j = input j, 2j+1 = input j+16), the order in which
@@ -45,7 +44,6 @@ namespace moex {
 constexpr int PF_NMAX = 192;     // tokens per tile (MMA N), multiple of 16
 constexpr int PF_BK = 64;        // inputs per k-step (one 128-byte swizzle row of FP16)
 constexpr int PF_NB_ST = 4;      // B (token) stages in shared memory
-constexpr int PF_BOXR = 64;      // token rows per TMA box
 constexpr int PF_NA_ST = 4;      // A (weight) stages in TMEM
 constexpr int PF_STAGE_B = PF_NMAX * PF_BK * 2;   // bytes of one B stage
 static_assert(PF_NB_ST == PF_NA_ST, "A and B stages advance together");
@@ -414,7 +412,6 @@ __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
-__device__ __forceinline__ int pf_mma_n(int nrows) { return (nrows + 15) & ~15; }
 
 // Named barrier over `count` threads that also ORs a flag across them, so
 // every participant takes the same branch afterwards.
@@ -444,11 +441,28 @@ struct PfSmem {
   }
 };
 
+// Token rows per TMA box: 64, or 32 for a CTA of a pair (it loads half of a
+// tile's rows, at most 96).
+template <bool PAIR>
+__host__ __device__ constexpr int pf_boxr() { return PAIR ? 32 : 64; }
+
+// MMA N of a tile of `nrows` tokens: a multiple of 16 (one CTA) or of 32 (a
+// pair, whose CTAs hold N/2 rows each).
+template <bool PAIR>
+__device__ __forceinline__ int pf_mma_n(int nrows) { return PAIR ? (nrows + 31) & ~31 : (nrows + 15) & ~15; }
+
 // EPI == 1: SwiGLU -> H (FP16).  EPI == 2: weighted combine into out.
 // EPI == 3: dense product, out[token][feature] = D (FP32, stride Hd).
 // WF: the weight format, IQ4_NL (raw stages of 4 k-steps) or Q8_0 (2).
-// CL == 2: clusters of two CTAs sharing each token stage (multicast); CL == 1: alone.
-template <int EPI, int CL, int WF>
+// PAIR: CTA pairs (clusters of two) on neighbouring feature tiles of the same
+// token tile share one M = 256 MMA (tcgen05 cta_group::2): each CTA
+// dequantises its own 128 weight rows into its own TMEM and loads its own
+// half of the token rows with plain TMA, so every SM writes and the MMA reads
+// half of the tile's token bytes per k-step; the even CTA issues the MMAs and
+// commits them to the barriers of both CTAs, and a forwarding thread of the
+// odd CTA tells it when that CTA's half of a stage is in place.  !PAIR: one
+// CTA, M = 128.
+template <int EPI, bool PAIR, int WF>
 __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __grid_constant__ CUtensorMap bmap,
                                                                      const __grid_constant__ CUtensorMap qmap,
                                                                      const __grid_constant__ CUtensorMap smap,
@@ -461,10 +475,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* b_full = bars;
   // k-step kc uses A stage and B stage kc % PF_NA_ST; one MMA commit per
-  // k-step releases both (with CL == 2, in both CTAs of the pair)
+  // k-step releases both (for a pair, in both CTAs)
   uint64_t* ab_empty = b_full + PF_NB_ST;
   uint64_t* a_full = ab_empty + PF_NB_ST;
-  uint64_t* d_full = a_full + PF_NA_ST + PF_NA_ST;
+  uint64_t* pair_full = a_full + PF_NA_ST;  // (even CTA of a pair) the odd CTA's stage is in place
+  uint64_t* d_full = pair_full + PF_NA_ST;
   uint64_t* d_empty = d_full + 2;
   uint64_t* done_bar = d_empty + 2;
   uint64_t* r_full = done_bar + 1;
@@ -472,19 +487,21 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   float* xbuf = reinterpret_cast<float*>(smem + L.xbuf);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.tmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+  constexpr int BOXR = pf_boxr<PAIR>();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < PF_NB_ST; ++i) {
       mbar_init(&b_full[i], 1);
-      mbar_init(&ab_empty[i], CL);  // the MMAs of every CTA of the cluster
+      mbar_init(&ab_empty[i], 1);   // the MMA thread's commit
     }
     for (int i = 0; i < PF_NA_ST; ++i) {
       mbar_init(&a_full[i], PF_DQ_WARPS);
+      mbar_init(&pair_full[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&d_full[i], 1);
-      mbar_init(&d_empty[i], 128);
+      mbar_init(&d_empty[i], PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs of a pair)
     }
     mbar_init(done_bar, 1);
     for (int i = 0; i < PF_NR_ST; ++i) {
@@ -498,34 +515,43 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
     tma_prefetch_desc(&smap);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, 512);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_holder, 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_holder, 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (CL == 2) cluster_sync_all();  // both CTAs' barriers are initialised before any multicast lands
+  if (PAIR) cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
   pdl_wait();  // tiles, tokens and (GEMM 2) H come from earlier kernels
   pdl_launch_dependents();
   // tiles 2p and 2p+1 (same expert and tokens, neighbouring feature tiles)
-  // go to the two CTAs of one cluster
-  const int rank = CL == 2 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int t0 = CL == 2 ? 2 * (blockIdx.x >> 1) + rank : blockIdx.x;
-  const int tstep = CL == 2 ? 2 * (gridDim.x >> 1) : gridDim.x;
+  // go to the two CTAs of one pair
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const int t0 = PAIR ? 2 * (blockIdx.x >> 1) + rank : blockIdx.x;
+  const int tstep = PAIR ? 2 * (gridDim.x >> 1) : gridDim.x;
   const int ntiles = *a.ntiles;
   const int KS = a.K / PF_BK;
 
   if (warp == 0) {
-    // ------------------------------------------------ B producer (TMA)
+    // ------------------------------------------------ B producer (TMA of this CTA's token rows)
     if (lane == 0) {
       int kc = 0;
       int4 nxt = t0 < ntiles ? a.tiles[t0] : make_int4(0, 0, 0, 0);
       for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
         const int4 tile = nxt;
         if (t + tstep < ntiles) nxt = a.tiles[t + tstep];  // read one tile ahead
-        const int nbox = (tile.w + PF_BOXR - 1) / PF_BOXR;
+        // a pair's even CTA loads tokens [0, N/2) of the tile, the odd one [N/2, N)
+        const int half = pf_mma_n<PAIR>(tile.w) / 2;
+        const int rows = PAIR ? half : tile.w;
+        const int row0 = tile.z + (PAIR ? rank * half : 0);
+        const int nbox = (rows + BOXR - 1) / BOXR;
         for (int ks = 0; ks < KS; ++ks, ++kc) {
           const int s = kc % PF_NB_ST;
           if (kc >= PF_NB_ST && !mbar_wait(&ab_empty[s], ((kc / PF_NB_ST) - 1) & 1, abort_flag)) {
@@ -533,15 +559,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
             flag_status(a.status, DEV_TIMEOUT_MMA);
             break;
           }
-          // the whole stage lands in this CTA (with CL == 2, half of the boxes from each CTA of the pair)
-          mbar_arrive_expect_tx(&b_full[s], nbox * PF_BOXR * PF_BK * 2);
-          for (int bx = rank; bx < nbox; bx += CL) {
-            uint8_t* dst = sb + s * PF_STAGE_B + bx * PF_BOXR * PF_BK * 2;
-            if (CL == 2)
-              tma_load_2d_mc(dst, &bmap, ks * PF_BK, tile.z + PF_BOXR * bx, &b_full[s], 0x3);
-            else
-              tma_load_2d(dst, &bmap, ks * PF_BK, tile.z + PF_BOXR * bx, &b_full[s]);
-          }
+          mbar_arrive_expect_tx(&b_full[s], nbox * BOXR * PF_BK * 2);
+          for (int bx = 0; bx < nbox; ++bx)
+            tma_load_2d(sb + s * PF_STAGE_B + bx * BOXR * PF_BK * 2, &bmap, ks * PF_BK, row0 + BOXR * bx, &b_full[s]);
         }
       }
       // after an abort, let the copies already issued land before the CTA exits
@@ -550,9 +570,34 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
           mbar_wait(&b_full[j % PF_NB_ST], (j / PF_NB_ST) & 1, nullptr);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
+  } else if (warp == 1 && PAIR && rank == 1) {
+    // ------------------------------------------------ odd CTA of a pair: stage forwarder
+    // once this CTA's A stage (TMEM) and B stage (shared memory) are in
+    // place, tell the even CTA, whose MMA reads both
     if (lane == 0) {
+      const uint32_t peer_full = cluster_addr(smem_u32(pair_full), 0);
+      int kc = 0;
+      for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
+        for (int ks = 0; ks < KS; ++ks, ++kc) {
+          const int s = kc % PF_NA_ST;
+          if (!mbar_wait(&a_full[s], (kc / PF_NA_ST) & 1, abort_flag) ||
+              !mbar_wait(&b_full[s], (kc / PF_NB_ST) & 1, abort_flag)) {
+            *abort_flag = 1;
+            flag_status(a.status, DEV_TIMEOUT_MMA);
+            break;
+          }
+          mbar_arrive_remote(peer_full + 8u * s);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer (one CTA, or the even CTA of a pair)
+    if (lane == 0) {
+      uint32_t ab_empty_peer = 0, d_full_peer = 0;
+      if constexpr (PAIR) {
+        ab_empty_peer = cluster_addr(smem_u32(ab_empty), 1);
+        d_full_peer = cluster_addr(smem_u32(d_full), 1);
+      }
       int kc = 0, ti = 0;
       bool issued_any = false;
       int4 nxt = t0 < ntiles ? a.tiles[t0] : make_int4(0, 0, 0, 0);
@@ -560,18 +605,23 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
         const int4 tile = nxt;
         if (t + tstep < ntiles) nxt = a.tiles[t + tstep];
         const int ab = ti & 1;
-        if (ti >= 2 && !mbar_wait(&d_empty[ab], ((ti >> 1) - 1) & 1, abort_flag)) {
-          *abort_flag = 1;
-          flag_status(a.status, DEV_TIMEOUT_MMA);
-          break;
+        if (ti >= 2) {
+          const bool ok = PAIR ? mbar_wait_cluster(&d_empty[ab], ((ti >> 1) - 1) & 1, abort_flag)
+                               : mbar_wait(&d_empty[ab], ((ti >> 1) - 1) & 1, abort_flag);
+          if (!ok) {
+            *abort_flag = 1;
+            flag_status(a.status, DEV_TIMEOUT_MMA);
+            break;
+          }
         }
         tc_fence_after();
-        const uint32_t idesc = idesc_f16_f32(128, pf_mma_n(tile.w));
+        const uint32_t idesc = idesc_f16_f32(PAIR ? 256 : 128, pf_mma_n<PAIR>(tile.w));
         const uint32_t dcol = tmem + ab * PF_NMAX;
         for (int ks = 0; ks < KS; ++ks, ++kc) {
           const int sa = kc % PF_NA_ST, sbk = kc % PF_NB_ST;
           if (!mbar_wait(&a_full[sa], (kc / PF_NA_ST) & 1, abort_flag) ||
-              !mbar_wait(&b_full[sbk], (kc / PF_NB_ST) & 1, abort_flag)) {
+              !mbar_wait(&b_full[sbk], (kc / PF_NB_ST) & 1, abort_flag) ||
+              (PAIR && !mbar_wait_cluster(&pair_full[sa], (kc / PF_NA_ST) & 1, abort_flag))) {
             *abort_flag = 1;
             flag_status(a.status, DEV_TIMEOUT_MMA);
             break;
@@ -580,21 +630,35 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
           const uint32_t baddr = smem_u32(sb + sbk * PF_STAGE_B);
 #pragma unroll
           for (int kk = 0; kk < PF_BK / 16; ++kk) {
-            mma_f16_ts(dcol, tmem + PF_ACOL + sa * 32 + kk * 8, smem_desc_sw128(baddr + kk * 32), idesc,
-                       (ks | kk) != 0);
+            const uint32_t acol = tmem + PF_ACOL + sa * 32 + kk * 8;
+            const uint64_t bdesc = smem_desc_sw128(baddr + kk * 32);
+            if constexpr (PAIR)
+              mma_f16_ts_pair(dcol, acol, bdesc, idesc, (ks | kk) != 0);
+            else
+              mma_f16_ts(dcol, acol, bdesc, idesc, (ks | kk) != 0);
           }
           issued_any = true;
-          if (CL == 2)
-            mma_commit_mc(&ab_empty[sa], 0x3);  // the shared B stage is refilled once both MMAs are done
-          else
+          if constexpr (PAIR) {
+            mma_commit_pair(smem_u32(&ab_empty[sa]));
+            mma_commit_pair(ab_empty_peer + 8u * sa);
+          } else {
             mma_commit(&ab_empty[sa]);
+          }
         }
         if (*abort_flag) break;
-        mma_commit(&d_full[ab]);
+        if constexpr (PAIR) {
+          mma_commit_pair(smem_u32(&d_full[ab]));
+          mma_commit_pair(d_full_peer + 8u * ab);
+        } else {
+          mma_commit(&d_full[ab]);
+        }
       }
       // make sure no MMA is still running before the TMEM is released
       if (issued_any) {
-        mma_commit(done_bar);
+        if constexpr (PAIR)
+          mma_commit_pair(smem_u32(done_bar));
+        else
+          mma_commit(done_bar);
         mbar_wait(done_bar, 0, nullptr);
       }
     }
@@ -700,6 +764,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   } else {
     // ------------------------------------------------ epilogue
     const int q = warp & 3;
+    // the accumulator is released to the MMA thread's CTA (the even CTA of a pair)
+    const uint32_t d_empty_mma = PAIR ? cluster_addr(smem_u32(d_empty), 0) : smem_u32(d_empty);
     int ti = 0;
     int4 nxt = t0 < ntiles ? a.tiles[t0] : make_int4(0, 0, 0, 0);
     for (int t = t0; t < ntiles; t += tstep, ++ti) {
@@ -761,15 +827,24 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
         }
       }
       tc_fence_before();
-      mbar_arrive(&d_empty[ab]);
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_remote(d_empty_mma + 8u * ab);
+        else
+          mbar_arrive(&d_empty[ab]);
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (CL == 2) cluster_sync_all();  // no multicast copy or commit of the partner is still in flight
+  if (PAIR) cluster_sync_all();  // the pair's MMAs, commits and remote arrivals are all done
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem, 512);
+    else
+      tmem_dealloc(tmem, 512);
   }
 }
 
@@ -793,13 +868,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D FP16 map over [rows][cols] (row pitch cols*2 bytes), box 64 x PF_BOXR, 128-byte swizzle.
-bool make_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
+// 2-D FP16 map over [rows][cols] (row pitch cols*2 bytes), box 64 inputs x
+// boxr rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int boxr) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
-  const cuuint32_t box[2] = {PF_BK, PF_BOXR};
+  const cuuint32_t box[2] = {PF_BK, static_cast<cuuint32_t>(boxr)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -875,11 +951,15 @@ int pf_grid(PfKernel kern, int cl, size_t smem) {
   return cached[slot];
 }
 
+// cl == 2: the CTA-pair kernel; cl == 1: single CTAs.
 template <int EPI>
 PfKernel pf_kernel(int cl, int fmt) {
-  if (fmt == MOEX_Q8_0) return cl == 2 ? prefill_gemm_kernel<EPI, 2, MOEX_Q8_0> : prefill_gemm_kernel<EPI, 1, MOEX_Q8_0>;
-  return cl == 2 ? prefill_gemm_kernel<EPI, 2, MOEX_IQ4_NL> : prefill_gemm_kernel<EPI, 1, MOEX_IQ4_NL>;
+  if (fmt == MOEX_Q8_0)
+    return cl == 2 ? prefill_gemm_kernel<EPI, true, MOEX_Q8_0> : prefill_gemm_kernel<EPI, false, MOEX_Q8_0>;
+  return cl == 2 ? prefill_gemm_kernel<EPI, true, MOEX_IQ4_NL> : prefill_gemm_kernel<EPI, false, MOEX_IQ4_NL>;
 }
+
+int pf_boxr_host(int cl) { return cl == 2 ? pf_boxr<true>() : pf_boxr<false>(); }
 
 cudaError_t launch_pf_gemm(PfKernel kern, int cl, size_t smem, cudaStream_t s, const CUtensorMap& bmap,
                            const CUtensorMap& qmap, const CUtensorMap& smap, const GemmArgs& args) {
@@ -936,9 +1016,11 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   __half* hs = reinterpret_cast<__half*>(wsb + off[7]);
   uint32_t* status = device_status_ptr();
 
+  // CTA pairs share each MMA when both GEMMs have an even number of feature tiles
+  const int cl = (I / 64) % 2 == 0 && (H / 128) % 2 == 0 ? 2 : 1;
   CUtensorMap m1, m2, q1, s1, q2, s2;
-  if (!make_map(&m1, xs, n, H) || !make_map(&m2, hs, n, I) || !make_weight_maps(&q1, &s1, gu) ||
-      !make_weight_maps(&q2, &s2, dn))
+  if (!make_map(&m1, xs, n, H, pf_boxr_host(cl)) || !make_map(&m2, hs, n, I, pf_boxr_host(cl)) ||
+      !make_weight_maps(&q1, &s1, gu) || !make_weight_maps(&q2, &s2, dn))
     return MOEX_ECUDA;
 
   int* hist = counts + E;
@@ -965,8 +1047,6 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
                  static_cast<int64_t>(T) * H / 4) != cudaSuccess)
     return MOEX_ECUDA;
   const PfSmem L;
-  // pairs share each token stage when both GEMMs have an even number of feature tiles
-  const int cl = (tl.F1 % 2 == 0 && tl.F2 % 2 == 0) ? 2 : 1;
   const PfKernel k1 = pf_kernel<1>(cl, gu->fmt);
   const PfKernel k2 = pf_kernel<2>(cl, dn->fmt);
   if (ensure_smem(reinterpret_cast<const void*>(k1), L.total) != cudaSuccess ||
@@ -1029,8 +1109,9 @@ moex_status launch_dense_prefill(const moex_qweight* W, const uint16_t* x, int T
   int* n1 = reinterpret_cast<int*>(wsb + off[1]);
   __half* xs = reinterpret_cast<__half*>(wsb + off[2]);
   uint32_t* status = device_status_ptr();
+  const int cl = F % 2 == 0 ? 2 : 1;
   CUtensorMap bm, qm, sm;
-  if (!make_map(&bm, xs, T, K) || !make_weight_maps(&qm, &sm, W)) return MOEX_ECUDA;
+  if (!make_map(&bm, xs, T, K, pf_boxr_host(cl)) || !make_weight_maps(&qm, &sm, W)) return MOEX_ECUDA;
   const int ntiles = pf_token_tiles(T) * F;
   if (launch_pdl(dense_tiles_kernel, dim3((ntiles + 255) / 256), dim3(256), 0, s, T, F, tiles, n1) != cudaSuccess)
     return MOEX_ECUDA;
@@ -1040,7 +1121,6 @@ moex_status launch_dense_prefill(const moex_qweight* W, const uint16_t* x, int T
                  static_cast<const float4*>(nullptr), static_cast<float4*>(nullptr), int64_t(0)) != cudaSuccess)
     return MOEX_ECUDA;
   const PfSmem L;
-  const int cl = F % 2 == 0 ? 2 : 1;
   const PfKernel kern = pf_kernel<3>(cl, W->fmt);
   if (ensure_smem(reinterpret_cast<const void*>(kern), L.total) != cudaSuccess) return MOEX_ECUDA;
   GemmArgs g = {};

@@ -105,29 +105,40 @@ def moe_prefill(gate_up, down, x_bf16: np.ndarray, ids: np.ndarray, w: np.ndarra
     Wdn = ExpertCache(down_fmt or fmt, down)
     inter = Wgu[int(ids[tokens[0], 0])].shape[0] // 2
     n = len(tokens)
-    out = np.zeros((n, hidden))
-    out_A = np.zeros((n, hidden))
     G = np.zeros((n, k, inter))
     U = np.zeros((n, k, inter))
     Hs = np.zeros((n, k, inter), dtype=np.float16)
     gu_A = np.zeros((n, k, 2 * inter))
+    O = np.zeros((n, k, hidden))
+    O_A = np.zeros((n, k, hidden))
+    Xh = fp16_rn(bf16_bits_to_f32(x_bf16[np.asarray(tokens)])).astype(np.float64)   # [n, hidden]
+    # every (token, slot) entry of each expert, experts in ascending order (the
+    # rows sorted by expert of #2356), so each expert's weights are expanded once
+    ent = {}
     for i, t in enumerate(tokens):
-        xh = fp16_rn(bf16_bits_to_f32(x_bf16[t])).astype(np.float64)
         for s in range(k):
-            e = int(ids[t, s])
-            wg = Wgu[e]
-            gu = wg @ xh
-            gu_A[i, s] = np.abs(wg) @ np.abs(xh)
-            G[i, s], U[i, s] = gu[:inter], gu[inter:]
-            if h_override is not None:
-                h = np.asarray(h_override(t, s), dtype=np.float16)
-            else:
-                h = fp16_rn(_moe.silu(gu[:inter]) * gu[inter:])
-            Hs[i, s] = h
-            wd = Wdn[e]
-            hf = h.astype(np.float64)
-            o = wd @ hf
-            oA = np.abs(wd) @ np.abs(hf)
-            out[i] += float(w[t, s]) * o
-            out_A[i] += abs(float(w[t, s])) * oA
+            ent.setdefault(int(ids[t, s]), []).append((i, s))
+    for e in sorted(ent):
+        ii = np.array([i for i, _ in ent[e]])
+        ss = np.array([s for _, s in ent[e]])
+        wg = Wgu[e]
+        gu = Xh[ii] @ wg.T                                   # [m, 2*inter], float64 sums
+        gu_A[ii, ss] = np.abs(Xh[ii]) @ np.abs(wg).T
+        G[ii, ss], U[ii, ss] = gu[:, :inter], gu[:, inter:]
+        if h_override is not None:
+            h = np.stack([np.asarray(h_override(tokens[i], s), dtype=np.float16) for i, s in ent[e]])
+        else:
+            h = fp16_rn(_moe.silu(gu[:, :inter]) * gu[:, inter:])
+        Hs[ii, ss] = h
+        wd = Wdn[e]
+        hf = h.astype(np.float64)
+        O[ii, ss] = hf @ wd.T
+        O_A[ii, ss] = np.abs(hf) @ np.abs(wd).T
+    # the top-k combine, slots in ascending order
+    out = np.zeros((n, hidden))
+    out_A = np.zeros((n, hidden))
+    for i, t in enumerate(tokens):
+        for s in range(k):
+            out[i] += float(w[t, s]) * O[i, s]
+            out_A[i] += abs(float(w[t, s])) * O_A[i, s]
     return dict(tokens=tokens, out=out, out_A=out_A, g=G, u=U, H=Hs, gu_A=gu_A)

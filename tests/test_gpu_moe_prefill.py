@@ -117,17 +117,21 @@ def test_prefill_small(T, E, k, hidden, inter):
     print(f"H mismatches {mism:.2e}, worst out error / tolerance {worst:.3f}")
 
 
-def test_prefill_expert_count_boundaries():
-    """Experts with 0, 1, 192, 193, 384 and 130 rows (k = 1): an empty
-    expert, a one-row tile, exactly one full tile, one row over, two full
-    tiles, and a ragged single tile; the routing is given, not drawn."""
-    counts = [0, 1, 192, 193, 384, 130]
+@pytest.mark.parametrize("inter", [64, 128])
+def test_prefill_expert_count_boundaries(inter):
+    """Experts with 0, 1, 192, 193, 384, 130, 16, 17 and 33 rows (k = 1): an
+    empty expert, a one-row tile, exactly one full tile, one row over, two
+    full tiles, a ragged single tile, and tiles around the pair split (16,
+    17 and 33 rows: a pair's MMA N is a multiple of 32, each CTA loading
+    half); the routing is given, not drawn.  inter 64 runs single CTAs (an
+    odd feature-tile count), inter 128 CTA pairs."""
+    counts = [0, 1, 192, 193, 384, 130, 16, 17, 33]
     E, T = len(counts), sum(counts)
     g = np.random.default_rng(17)
     ids = np.repeat(np.arange(E), counts)
     g.shuffle(ids)
     w = g.uniform(0.2, 1.0, size=T).astype(np.float32)
-    mism, worst = run(T, E, 1, 256, 64, seed=29, routing=(ids.reshape(T, 1), w.reshape(T, 1)))
+    mism, worst = run(T, E, 1, 256, inter, seed=29, routing=(ids.reshape(T, 1), w.reshape(T, 1)))
     print(f"H mismatches {mism:.2e}, worst out error / tolerance {worst:.3f}")
 
 
@@ -138,7 +142,17 @@ def test_prefill_q8_0_gate_up():
 
 
 def test_prefill_workload_full_size_sampled():
-    """8192 tokens, 128 experts top-8, hidden 2560, inter 1536; the oracle
-    recomputes 6 sampled tokens (48 entries) and the whole sort."""
-    mism, worst = run(8192, 128, 8, 2560, 1536, seed=0, sample=[0, 1, 777, 4096, 8000, 8191])
-    print(f"H mismatches {mism:.2e}, worst out error / tolerance {worst:.3f}")
+    """8192 tokens, 128 experts top-8, hidden 2560, inter 1536.  The whole
+    sort is checked; the oracle recomputes the tokens of every expert's first
+    and last sorted row (so each expert's first tile and ragged last tile
+    are compared element by element over all features) plus 6 fixed tokens:
+    about 250 tokens, 2000 entries."""
+    T, E, k, seed = 8192, 128, 8, 0
+    ids, _ = om.route_topk(synth.router_logits(synth.rng(seed + 1), T, E), k)
+    order, off = op.sort_entries(ids, E)
+    edge = [order[off[e]] // k for e in range(E) if off[e + 1] > off[e]]
+    edge += [order[off[e + 1] - 1] // k for e in range(E) if off[e + 1] > off[e]]
+    sample = sorted(set(int(t) for t in edge) | {0, 1, 777, 4096, 8000, 8191})
+    assert len(sample) >= 128
+    mism, worst = run(T, E, k, 2560, 1536, seed=seed, sample=sample)
+    print(f"{len(sample)} tokens: H mismatches {mism:.2e}, worst out error / tolerance {worst:.3f}")
