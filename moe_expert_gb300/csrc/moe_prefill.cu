@@ -606,9 +606,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
         if (t + tstep < ntiles) nxt = a.tiles[t + tstep];
         const int ab = ti & 1;
         if (ti >= 2) {
-          const bool ok = PAIR ? mbar_wait_cluster(&d_empty[ab], ((ti >> 1) - 1) & 1, abort_flag)
-                               : mbar_wait(&d_empty[ab], ((ti >> 1) - 1) & 1, abort_flag);
-          if (!ok) {
+          if (!mbar_wait(&d_empty[ab], ((ti >> 1) - 1) & 1, abort_flag)) {
             *abort_flag = 1;
             flag_status(a.status, DEV_TIMEOUT_MMA);
             break;
@@ -621,7 +619,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
           const int sa = kc % PF_NA_ST, sbk = kc % PF_NB_ST;
           if (!mbar_wait(&a_full[sa], (kc / PF_NA_ST) & 1, abort_flag) ||
               !mbar_wait(&b_full[sbk], (kc / PF_NB_ST) & 1, abort_flag) ||
-              (PAIR && !mbar_wait_cluster(&pair_full[sa], (kc / PF_NA_ST) & 1, abort_flag))) {
+              (PAIR && !mbar_wait(&pair_full[sa], (kc / PF_NA_ST) & 1, abort_flag))) {
             *abort_flag = 1;
             flag_status(a.status, DEV_TIMEOUT_MMA);
             break;

@@ -176,35 +176,13 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-// Arrives on an mbarrier of any CTA of the cluster, releasing this thread's
-// prior writes at cluster scope.
+// Arrives on an mbarrier of any CTA of the cluster (default semantics:
+// release at CTA scope, no cluster-wide fence).  The pair kernel uses it only
+// after the data it announces is complete: TMEM stores waited for with
+// tcgen05.wait::st, TMA copies observed through their own mbarrier, TMEM
+// loads waited for with tcgen05.wait::ld.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
-}
-
-// mbar_wait for a barrier that threads of another CTA of the cluster arrive
-// on: the completed phase acquires their writes at cluster scope.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (abort && *abort) return false;
-      if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
-    }
-  }
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -145,14 +145,17 @@ def test_prefill_workload_full_size_sampled():
     """8192 tokens, 128 experts top-8, hidden 2560, inter 1536.  The whole
     sort is checked; the oracle recomputes the tokens of every expert's first
     and last sorted row (so each expert's first tile and ragged last tile
-    are compared element by element over all features) plus 6 fixed tokens:
-    about 250 tokens, 2000 entries."""
+    are compared element by element over all features), 6 fixed tokens and
+    64 drawn ones: about 150 tokens, 1200 entries."""
     T, E, k, seed = 8192, 128, 8, 0
     ids, _ = om.route_topk(synth.router_logits(synth.rng(seed + 1), T, E), k)
     order, off = op.sort_entries(ids, E)
     edge = [order[off[e]] // k for e in range(E) if off[e + 1] > off[e]]
     edge += [order[off[e + 1] - 1] // k for e in range(E) if off[e + 1] > off[e]]
-    sample = sorted(set(int(t) for t in edge) | {0, 1, 777, 4096, 8000, 8191})
+    # (the first rows of most experts fall on the first few tokens and the
+    # last rows on the last few, so 64 more tokens are drawn)
+    extra = np.random.default_rng(11).choice(T, 64, replace=False)
+    sample = sorted(set(int(t) for t in edge) | {0, 1, 777, 4096, 8000, 8191} | set(int(t) for t in extra))
     assert len(sample) >= 128
     mism, worst = run(T, E, k, 2560, 1536, seed=seed, sample=sample)
     print(f"{len(sample)} tokens: H mismatches {mism:.2e}, worst out error / tolerance {worst:.3f}")
