@@ -41,17 +41,20 @@
 
 namespace moex {
 
-constexpr int PF_NMAX = 192;     // tokens per tile (MMA N), multiple of 16
+constexpr int PF_SUBN = 192;     // tokens of one MMA sub-tile (one TMEM accumulator slot)
+constexpr int PF_CAP_PAIR = 384; // tokens of a tile for CTA pairs: two sub-tiles
+constexpr int PF_CAP_ONE = 192;  // tokens of a tile for single CTAs: one sub-tile
 constexpr int PF_BK = 64;        // inputs per k-step (one 128-byte swizzle row of FP16)
 constexpr int PF_NB_ST = 4;      // B (token) stages in shared memory
 constexpr int PF_NA_ST = 4;      // A (weight) stages in TMEM
-constexpr int PF_STAGE_B = PF_NMAX * PF_BK * 2;   // bytes of one B stage
+constexpr int PF_STAGE_B = 192 * PF_BK * 2;       // bytes of one B stage: at most 192 token rows a CTA
 static_assert(PF_NB_ST == PF_NA_ST, "A and B stages advance together");
-constexpr int PF_ACOL = 2 * PF_NMAX;              // first TMEM column of the A stages
+constexpr int PF_ACOL = 2 * PF_SUBN;              // first TMEM column of the A stages (after two slots)
 constexpr int PF_DQ_WARPS = 8;   // dequantising warps: two per TMEM lane quarter, one IQ4_NL block each
 constexpr int PF_DQ0 = 3;        // first dequantising warp
-constexpr int PF_THREADS = (3 + PF_DQ_WARPS + 4) * 32;  // warp 0 B TMA, 1 MMA + TMEM, 2 A TMA, dequant, 4 epilogue
 constexpr int PF_EPI0 = PF_DQ0 + PF_DQ_WARPS;           // first epilogue warp
+constexpr int PF_EPI_WARPS = 8;  // epilogue warps: two per TMEM lane quarter, alternate 32-column chunks
+constexpr int PF_THREADS = (PF_EPI0 + PF_EPI_WARPS) * 32;  // warp 0 B TMA, 1 MMA + TMEM, 2 A TMA, dequant, epilogue
 // Raw weight stages: the IQ4_NL bytes of 128 rows x 4 k-steps (8 blocks a
 // row), two boxes of 64 rows x 128 bytes with the 128-byte swizzle, then
 // their FP16 scales, two boxes of 64 rows x 16 bytes.
@@ -75,9 +78,19 @@ struct PrefillTiles {
   int* n1;      // number of GEMM 1 tiles; n1[1] GEMM 2 tiles, n1[2] placed rows
   int* n2;
   int F1, F2;   // feature tiles per expert (I/64, H/128)
+  int cap;      // most token rows a tile takes (PF_CAP_ONE for the MoE layer)
 };
 
-__host__ __device__ inline int pf_token_tiles(int n) { return (n + PF_NMAX - 1) / PF_NMAX; }
+// An expert's n rows are cut into ceil(n / cap) token tiles of balanced size
+// (the first n % nt tiles one row longer), so every tile of an expert does
+// about the same MMA work per dequantised weight stage.
+__host__ __device__ inline int pf_token_tiles(int n, int cap) { return (n + cap - 1) / cap; }
+__host__ __device__ inline void pf_tile_span(int n, int cap, int t, int* r0, int* rows) {
+  const int nt = pf_token_tiles(n, cap);
+  const int base = n / nt, rem = n % nt;
+  *r0 = t * base + (t < rem ? t : rem);
+  *rows = base + (t < rem ? 1 : 0);
+}
 
 constexpr int PF_MAX_SEGS = 1024;   // at most this many histogram segments
 
@@ -159,7 +172,7 @@ __global__ void __launch_bounds__(1024) prefill_scan_kernel(int n, int E, int* _
       for (int sg = 0; sg < S; ++sg) v += hist[static_cast<int64_t>(sg) * E + e];
     c[i] = v;
     csum += v;
-    tsum += pf_token_tiles(v);
+    tsum += pf_token_tiles(v, tl.cap);
   }
   int off = csum, tb = tsum;
   const int placed = block_exscan(off, red);
@@ -186,13 +199,13 @@ __global__ void __launch_bounds__(1024) prefill_scan_kernel(int n, int E, int* _
       run += h;
     }
     off += c[i];
-    tb += pf_token_tiles(c[i]);
+    tb += pf_token_tiles(c[i], tl.cap);
   }
 }
 
 // Both tile lists, one thread per tile: token tile g belongs to the last
-// expert e with etb[e] <= g; its ceil(n_e / 192) token tiles take 192 rows
-// each, the last one the rest.
+// expert e with etb[e] <= g; its ceil(n_e / cap) token tiles split the
+// expert's rows evenly.
 __global__ void __launch_bounds__(256) prefill_tiles_kernel(int E, const int* __restrict__ counts,
                                                             const int* __restrict__ eoff, const int* __restrict__ etb,
                                                             PrefillTiles tl) {
@@ -211,21 +224,18 @@ __global__ void __launch_bounds__(256) prefill_tiles_kernel(int E, const int* __
     if (etb[mid] <= g) lo = mid; else hi = mid - 1;
   }
   const int e = lo;
-  const int64_t ne = counts[e];
-  const int64_t tt = g - etb[e];
-  // full tiles of PF_NMAX rows and one ragged last tile: every token box but
-  // the last of an expert is full, so no loaded row is padding
-  const int r0 = eoff[e] + static_cast<int>(tt * PF_NMAX);
-  const int r1 = eoff[e] + static_cast<int>((tt + 1) * PF_NMAX < ne ? (tt + 1) * PF_NMAX : ne);
-  (first ? tl.t1 : tl.t2)[j] = make_int4(e, f, r0, r1 - r0);
+  int r0, rows;
+  pf_tile_span(counts[e], tl.cap, g - etb[e], &r0, &rows);
+  (first ? tl.t1 : tl.t2)[j] = make_int4(e, f, eoff[e] + r0, rows);
 }
 
-// Dense product: token tiles of 192 rows (the last one ragged) times
-// feature tiles of 128 rows, all of matrix 0; n1[0] = tiles, n1[2] = rows.
-__global__ void __launch_bounds__(256) dense_tiles_kernel(int T, int F, int4* __restrict__ tiles, int* __restrict__ n1) {
+// Dense product: balanced token tiles of at most `cap` rows times feature
+// tiles of 128 rows, all of matrix 0; n1[0] = tiles, n1[2] = rows.
+__global__ void __launch_bounds__(256) dense_tiles_kernel(int T, int F, int cap, int4* __restrict__ tiles,
+                                                          int* __restrict__ n1) {
   pdl_wait();
   pdl_launch_dependents();
-  const int ntt = pf_token_tiles(T);
+  const int ntt = pf_token_tiles(T, cap);
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i == 0) {
     n1[0] = ntt * F;
@@ -235,8 +245,9 @@ __global__ void __launch_bounds__(256) dense_tiles_kernel(int T, int F, int4* __
   }
   if (i >= ntt * F) return;
   const int tt = i / F, f = i % F;
-  const int r0 = tt * PF_NMAX;
-  tiles[i] = make_int4(0, f, r0, (T - r0) < PF_NMAX ? (T - r0) : PF_NMAX);
+  int r0, rows;
+  pf_tile_span(T, cap, tt, &r0, &rows);
+  tiles[i] = make_int4(0, f, r0, rows);
 }
 
 // One warp per segment, entries in order, 32 at a time: equal experts are
@@ -413,27 +424,14 @@ __device__ __forceinline__ void red_add_f32(float* p, float v) {
 }
 
 
-// Named barrier over `count` threads that also ORs a flag across them, so
-// every participant takes the same branch afterwards.
-__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool flag) {
-  uint32_t out;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(out)
-      : "r"(static_cast<uint32_t>(flag)), "r"(id), "r"(count)
-      : "memory");
-  return out != 0;
-}
-
 struct PfSmem {
-  int b, raw, bars, xbuf, tmem, abort_flag, total;
+  int b, raw, bars, tmem, abort_flag, total;
   __host__ __device__ PfSmem() {
     int o = 0;
     b = o; o += PF_NB_ST * PF_STAGE_B;                          // 1024-aligned (dynamic smem base)
     raw = o; o += PF_NR_ST * PF_RAW_STAGE;                      // 1024-aligned
     bars = o; o += 8 * (2 * PF_NB_ST + 2 * PF_NA_ST + 2 * PF_NR_ST + 4 + 1);
     o = (o + 15) & ~15;
-    xbuf = o; o += 2 * 32 * 33 * 4;
     tmem = o; o += 16;
     abort_flag = o; o += 16;
     total = o + 1024;                                          // slack for aligning the base
@@ -442,26 +440,69 @@ struct PfSmem {
 };
 
 // Token rows per TMA box: 64, or 32 for a CTA of a pair (it loads half of a
-// tile's rows, at most 96).
+// sub-tile's rows, at most 96).
 template <bool PAIR>
 __host__ __device__ constexpr int pf_boxr() { return PAIR ? 32 : 64; }
 
-// MMA N of a tile of `nrows` tokens: a multiple of 16 (one CTA) or of 32 (a
-// pair, whose CTAs hold N/2 rows each).
+// MMA N of a sub-tile of `nrows` tokens: a multiple of 16 (one CTA) or of 32
+// (a pair, whose CTAs hold N/2 rows each).
 template <bool PAIR>
 __device__ __forceinline__ int pf_mma_n(int nrows) { return PAIR ? (nrows + 31) & ~31 : (nrows + 15) & ~15; }
+
+// How a tile of `rows` tokens is laid out: sub-tile h (h = 0, 1) covers tile
+// rows [start[h], start[h] + rows[h]) with MMA width n[h] into TMEM slot h
+// (columns h * PF_SUBN ..); in a B stage this CTA's rows of sub-tile h start
+// at row off[h] and take nbox[h] TMA boxes.  A pair's even CTA holds rows
+// [0, n/2) of each sub-tile and the odd CTA rows [n/2, n).
+template <bool PAIR>
+struct PfSubTiles {
+  int start[2], rows[2], n[2], off[2], nbox[2];
+  __device__ __forceinline__ PfSubTiles(int tile_rows) {
+    constexpr int BOXR = pf_boxr<PAIR>();
+    // one sub-tile up to PF_SUBN rows, else two of about half the rows (the
+    // first a multiple of 32, at most PF_SUBN), so neither MMA is narrow
+    const int half = (((tile_rows + 1) / 2) + 31) & ~31;
+    rows[0] = tile_rows <= PF_SUBN ? tile_rows : (half < PF_SUBN ? half : PF_SUBN);
+    rows[1] = tile_rows - rows[0];
+    start[0] = 0;
+    start[1] = rows[0];
+    off[0] = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      n[h] = rows[h] > 0 ? pf_mma_n<PAIR>(rows[h]) : 0;
+      const int held = PAIR ? n[h] / 2 : rows[h];
+      nbox[h] = (held + BOXR - 1) / BOXR;
+    }
+    off[1] = nbox[0] * BOXR;
+  }
+};
+
+// Feature tile row of TMEM lane m in GEMM 1 (rows 0..63 gate, 64..127 up in
+// the raw weight stage).  The lanes of warp q hold, for 16 features j of a
+// 32-feature block and the 16 features j + 16 of the same block, the gate
+// row (lane bit 3 clear) and the up row (bit 3 set): gate and up of a
+// feature are lanes l and l ^ 8, features j and j + 16 lanes l and l ^ 16.
+__device__ __forceinline__ int pf_gu_feature(int m) {
+  const int q = m >> 5, l = m & 31;
+  return 32 * (q >> 1) + 8 * (q & 1) + (l & 7) + 16 * (l >> 4);
+}
+__device__ __forceinline__ int pf_gu_raw_row(int m) {
+  return ((m >> 3) & 1) * 64 + pf_gu_feature(m);
+}
 
 // EPI == 1: SwiGLU -> H (FP16).  EPI == 2: weighted combine into out.
 // EPI == 3: dense product, out[token][feature] = D (FP32, stride Hd).
 // WF: the weight format, IQ4_NL (raw stages of 4 k-steps) or Q8_0 (2).
 // PAIR: CTA pairs (clusters of two) on neighbouring feature tiles of the same
-// token tile share one M = 256 MMA (tcgen05 cta_group::2): each CTA
-// dequantises its own 128 weight rows into its own TMEM and loads its own
-// half of the token rows with plain TMA, so every SM writes and the MMA reads
-// half of the tile's token bytes per k-step; the even CTA issues the MMAs and
-// commits them to the barriers of both CTAs, and a forwarding thread of the
-// odd CTA tells it when that CTA's half of a stage is in place.  !PAIR: one
-// CTA, M = 128.
+// token tile share M = 256 MMAs (tcgen05 cta_group::2): each CTA dequantises
+// its own 128 weight rows into its own TMEM and loads its own half of the
+// token rows with plain TMA, so every SM writes and the MMA reads half of the
+// tile's token bytes per k-step; the even CTA issues the MMAs and commits them
+// to the barriers of both CTAs, and a forwarding thread of the odd CTA tells
+// it when that CTA's half of a stage is in place.  A pair's tile has up to
+// 384 tokens in two sub-tiles (two accumulator slots), so each dequantised
+// weight stage feeds twice the MMA work of a 192-token tile.  !PAIR: one CTA,
+// M = 128, tiles of up to 192 tokens.
 template <int EPI, bool PAIR, int WF>
 __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __grid_constant__ CUtensorMap bmap,
                                                                      const __grid_constant__ CUtensorMap qmap,
@@ -477,14 +518,16 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   // k-step kc uses A stage and B stage kc % PF_NA_ST; one MMA commit per
   // k-step releases both (for a pair, in both CTAs)
   uint64_t* ab_empty = b_full + PF_NB_ST;
-  uint64_t* a_full = ab_empty + PF_NB_ST;
-  uint64_t* pair_full = a_full + PF_NA_ST;  // (even CTA of a pair) the odd CTA's stage is in place
-  uint64_t* d_full = pair_full + PF_NA_ST;
-  uint64_t* d_empty = d_full + 2;
+  // full[s] (on the CTA that issues the MMAs): the A stage is in TMEM in
+  // every CTA of the pair (each dequantising warp arrives; the odd CTA's
+  // remotely) and the odd CTA's B stage is in place (its forwarder arrives);
+  // the issuing CTA's own B stage is b_full[s]
+  uint64_t* full = ab_empty + PF_NB_ST;
+  uint64_t* d_full = full + 2 * PF_NA_ST;   // accumulator slot h holds a finished sub-tile
+  uint64_t* d_empty = d_full + 2;           // accumulator slot h has been read by every epilogue warp
   uint64_t* done_bar = d_empty + 2;
   uint64_t* r_full = done_bar + 1;
   uint64_t* r_empty = r_full + PF_NR_ST;
-  float* xbuf = reinterpret_cast<float*>(smem + L.xbuf);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.tmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
   constexpr int BOXR = pf_boxr<PAIR>();
@@ -495,13 +538,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
       mbar_init(&b_full[i], 1);
       mbar_init(&ab_empty[i], 1);   // the MMA thread's commit
     }
-    for (int i = 0; i < PF_NA_ST; ++i) {
-      mbar_init(&a_full[i], PF_DQ_WARPS);
-      mbar_init(&pair_full[i], 1);
-    }
+    for (int i = 0; i < PF_NA_ST; ++i) mbar_init(&full[i], PAIR ? 2 * PF_DQ_WARPS + 1 : PF_DQ_WARPS);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&d_full[i], 1);
-      mbar_init(&d_empty[i], PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs of a pair)
+      mbar_init(&d_empty[i], (PAIR ? 2 : 1) * PF_EPI_WARPS);  // every epilogue warp (of both CTAs of a pair)
     }
     mbar_init(done_bar, 1);
     for (int i = 0; i < PF_NR_ST; ++i) {
@@ -547,11 +587,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
       for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
         const int4 tile = nxt;
         if (t + tstep < ntiles) nxt = a.tiles[t + tstep];  // read one tile ahead
-        // a pair's even CTA loads tokens [0, N/2) of the tile, the odd one [N/2, N)
-        const int half = pf_mma_n<PAIR>(tile.w) / 2;
-        const int rows = PAIR ? half : tile.w;
-        const int row0 = tile.z + (PAIR ? rank * half : 0);
-        const int nbox = (rows + BOXR - 1) / BOXR;
+        const PfSubTiles<PAIR> st(tile.w);
+        int src[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) src[h] = tile.z + st.start[h] + (PAIR ? rank * (st.n[h] / 2) : 0);
+        const uint32_t bytes = (st.nbox[0] + st.nbox[1]) * BOXR * PF_BK * 2;
         for (int ks = 0; ks < KS; ++ks, ++kc) {
           const int s = kc % PF_NB_ST;
           if (kc >= PF_NB_ST && !mbar_wait(&ab_empty[s], ((kc / PF_NB_ST) - 1) & 1, abort_flag)) {
@@ -559,9 +599,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
             flag_status(a.status, DEV_TIMEOUT_MMA);
             break;
           }
-          mbar_arrive_expect_tx(&b_full[s], nbox * BOXR * PF_BK * 2);
-          for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(sb + s * PF_STAGE_B + bx * BOXR * PF_BK * 2, &bmap, ks * PF_BK, row0 + BOXR * bx, &b_full[s]);
+          mbar_arrive_expect_tx(&b_full[s], bytes);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            for (int bx = 0; bx < st.nbox[h]; ++bx)
+              tma_load_2d(sb + s * PF_STAGE_B + (st.off[h] + bx * BOXR) * PF_BK * 2, &bmap, ks * PF_BK,
+                          src[h] + BOXR * bx, &b_full[s]);
         }
       }
       // after an abort, let the copies already issued land before the CTA exits
@@ -571,17 +614,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
       }
     }
   } else if (warp == 1 && PAIR && rank == 1) {
-    // ------------------------------------------------ odd CTA of a pair: stage forwarder
-    // once this CTA's A stage (TMEM) and B stage (shared memory) are in
-    // place, tell the even CTA, whose MMA reads both
+    // ------------------------------------------------ odd CTA of a pair: B stage forwarder
+    // once this CTA's B stage (its half of the token rows) has landed, tell
+    // the even CTA, whose MMA reads it (the A stage is announced by the
+    // dequantising warps themselves)
     if (lane == 0) {
-      const uint32_t peer_full = cluster_addr(smem_u32(pair_full), 0);
+      const uint32_t peer_full = cluster_addr(smem_u32(full), 0);
       int kc = 0;
       for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
         for (int ks = 0; ks < KS; ++ks, ++kc) {
-          const int s = kc % PF_NA_ST;
-          if (!mbar_wait(&a_full[s], (kc / PF_NA_ST) & 1, abort_flag) ||
-              !mbar_wait(&b_full[s], (kc / PF_NB_ST) & 1, abort_flag)) {
+          const int s = kc % PF_NB_ST;
+          if (!mbar_wait(&b_full[s], (kc / PF_NB_ST) & 1, abort_flag)) {
             *abort_flag = 1;
             flag_status(a.status, DEV_TIMEOUT_MMA);
             break;
@@ -598,57 +641,77 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
         ab_empty_peer = cluster_addr(smem_u32(ab_empty), 1);
         d_full_peer = cluster_addr(smem_u32(d_full), 1);
       }
-      int kc = 0, ti = 0;
+      int kc = 0;
+      int nsub = 0;  // sub-tiles so far: sub-tile number i accumulates in slot i & 1 (its use i >> 1)
       bool issued_any = false;
       int4 nxt = t0 < ntiles ? a.tiles[t0] : make_int4(0, 0, 0, 0);
-      for (int t = t0; t < ntiles && !*abort_flag; t += tstep, ++ti) {
+      for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
         const int4 tile = nxt;
         if (t + tstep < ntiles) nxt = a.tiles[t + tstep];
-        const int ab = ti & 1;
-        if (ti >= 2) {
-          if (!mbar_wait(&d_empty[ab], ((ti >> 1) - 1) & 1, abort_flag)) {
-            *abort_flag = 1;
-            flag_status(a.status, DEV_TIMEOUT_MMA);
-            break;
-          }
+        const PfSubTiles<PAIR> st(tile.w);
+        // everything the k-loop needs, computed once a tile: per sub-tile the
+        // instruction descriptor, the D column and the B descriptor of stage 0
+        // (a stage or a 16-input step only adds to its 14-bit address field)
+        const int nh = st.n[1] > 0 ? 2 : 1;
+        uint32_t idesc[2], dcol[2];
+        uint64_t bdesc[2];
+        int sub[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          sub[h] = nsub + h;
+          idesc[h] = idesc_f16_f32(PAIR ? 256 : 128, st.n[h] > 0 ? st.n[h] : 16);
+          dcol[h] = tmem + (sub[h] & 1) * PF_SUBN;
+          bdesc[h] = smem_desc_sw128(smem_u32(sb) + st.off[h] * PF_BK * 2);
         }
-        tc_fence_after();
-        const uint32_t idesc = idesc_f16_f32(PAIR ? 256 : 128, pf_mma_n<PAIR>(tile.w));
-        const uint32_t dcol = tmem + ab * PF_NMAX;
+        // the slots' previous sub-tiles must have been read out first
+        bool ok = true;
+        for (int h = 0; h < nh && ok; ++h)
+          if (sub[h] >= 2) ok = mbar_wait(&d_empty[sub[h] & 1], ((sub[h] >> 1) - 1) & 1, abort_flag);
+        if (!ok) {
+          *abort_flag = 1;
+          flag_status(a.status, DEV_TIMEOUT_MMA);
+          break;
+        }
         for (int ks = 0; ks < KS; ++ks, ++kc) {
-          const int sa = kc % PF_NA_ST, sbk = kc % PF_NB_ST;
-          if (!mbar_wait(&a_full[sa], (kc / PF_NA_ST) & 1, abort_flag) ||
-              !mbar_wait(&b_full[sbk], (kc / PF_NB_ST) & 1, abort_flag) ||
-              (PAIR && !mbar_wait(&pair_full[sa], (kc / PF_NA_ST) & 1, abort_flag))) {
+          const int s = kc % PF_NA_ST;
+          if (!mbar_wait(&b_full[s], (kc / PF_NB_ST) & 1, abort_flag) ||
+              !mbar_wait(&full[s], (kc / PF_NA_ST) & 1, abort_flag)) {
             *abort_flag = 1;
             flag_status(a.status, DEV_TIMEOUT_MMA);
             break;
           }
           tc_fence_after();
-          const uint32_t baddr = smem_u32(sb + sbk * PF_STAGE_B);
+          const uint32_t acol = tmem + PF_ACOL + s * 32;
+          const uint64_t boff = static_cast<uint64_t>((s * PF_STAGE_B) >> 4);
+          for (int h = 0; h < nh; ++h) {
 #pragma unroll
-          for (int kk = 0; kk < PF_BK / 16; ++kk) {
-            const uint32_t acol = tmem + PF_ACOL + sa * 32 + kk * 8;
-            const uint64_t bdesc = smem_desc_sw128(baddr + kk * 32);
-            if constexpr (PAIR)
-              mma_f16_ts_pair(dcol, acol, bdesc, idesc, (ks | kk) != 0);
-            else
-              mma_f16_ts(dcol, acol, bdesc, idesc, (ks | kk) != 0);
+            for (int kk = 0; kk < PF_BK / 16; ++kk) {
+              if constexpr (PAIR)
+                mma_f16_ts_pair(dcol[h], acol + kk * 8, bdesc[h] + boff + 2 * kk, idesc[h], (ks | kk) != 0);
+              else
+                mma_f16_ts(dcol[h], acol + kk * 8, bdesc[h] + boff + 2 * kk, idesc[h], (ks | kk) != 0);
+            }
           }
           issued_any = true;
           if constexpr (PAIR) {
-            mma_commit_pair(smem_u32(&ab_empty[sa]));
-            mma_commit_pair(ab_empty_peer + 8u * sa);
+            mma_commit_pair(smem_u32(&ab_empty[s]));
+            mma_commit_pair(ab_empty_peer + 8u * s);
           } else {
-            mma_commit(&ab_empty[sa]);
+            mma_commit(&ab_empty[s]);
           }
         }
         if (*abort_flag) break;
-        if constexpr (PAIR) {
-          mma_commit_pair(smem_u32(&d_full[ab]));
-          mma_commit_pair(d_full_peer + 8u * ab);
-        } else {
-          mma_commit(&d_full[ab]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (st.n[h] == 0) continue;
+          const int sl = sub[h] & 1;
+          if constexpr (PAIR) {
+            mma_commit_pair(smem_u32(&d_full[sl]));
+            mma_commit_pair(d_full_peer + 8u * sl);
+          } else {
+            mma_commit(&d_full[sl]);
+          }
+          ++nsub;
         }
       }
       // make sure no MMA is still running before the TMEM is released
@@ -671,7 +734,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
         const int4 tile = nxt;
         if (t + tstep < ntiles) nxt = a.tiles[t + tstep];  // read one tile ahead
         const int64_t base = static_cast<int64_t>(tile.x) * a.rows_per_expert;
-        // weight rows of A rows 0..63 and 64..127: gate and up features (GEMM 1) or 128 outputs (GEMM 2)
+        // weight rows of raw rows 0..63 and 64..127: gate and up features (GEMM 1) or 128 outputs (GEMM 2)
         const int y0 = static_cast<int>(EPI == 1 ? base + tile.y * 64 : base + tile.y * 128);
         const int y1 = static_cast<int>(EPI == 1 ? base + a.I + tile.y * 64 : base + tile.y * 128 + 64);
         for (int g = 0; g < ngroups; ++g, ++rc) {
@@ -702,12 +765,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
     // of each 64-input k-step (TMEM columns 16h .. 16h+15 of the stage).
     const int q = warp & 3;
     const int h = (warp - PF_DQ0) >> 2;
-    const int m = 32 * q + lane;  // A row = TMEM lane
-    // this row's bytes in a raw stage: 128-byte rows, 16-byte chunk c stored at chunk c ^ (row & 7)
-    const int qoff = (m >> 6) * 64 * 128 + (m & 63) * 128;
-    const int soff = PF_RAW_QS + (m >> 6) * 64 * 16 + (m & 63) * 16;
+    const int m = 32 * q + lane;                          // A row = TMEM lane
+    const int rr = EPI == 1 ? pf_gu_raw_row(m) : m;       // its row in the raw stage
+    // raw stage rows: 128 bytes, 16-byte chunk c stored at chunk c ^ (row & 7)
+    const int qoff = (rr >> 6) * 64 * 128 + (rr & 63) * 128;
+    const int soff = PF_RAW_QS + (rr >> 6) * 64 * 16 + (rr & 63) * 16;
     constexpr int RKS = pf_raw_ks(WF);
     const int ngroups = (KS + RKS - 1) / RKS;
+    const uint32_t full_mma = PAIR ? cluster_addr(smem_u32(full), 0) : 0;  // the issuing CTA's full barriers
     int kc = 0, rc = 0;
     for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
       for (int g = 0; g < ngroups && !*abort_flag; ++g, ++rc) {
@@ -727,7 +792,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
         for (int j = 0; j < RKS; ++j)
 #pragma unroll
           for (int c = 0; c < NCH; ++c)
-            if (j < nk) qv[j][c] = *reinterpret_cast<const uint4*>(st + qoff + (((NCH * (2 * j + h) + c) ^ (m & 7)) << 4));
+            if (j < nk) qv[j][c] = *reinterpret_cast<const uint4*>(st + qoff + (((NCH * (2 * j + h) + c) ^ (rr & 7)) << 4));
         __syncwarp();
         if (lane == 0) mbar_arrive(&r_empty[r]);  // the raw bytes are in registers
         const uint32_t sw[4] = {scv.x, scv.y, scv.z, scv.w};
@@ -754,83 +819,89 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[s]);  // the warp's 32 rows of this block are in TMEM
+          if (lane == 0) {  // the warp's 32 rows of this block are in TMEM
+            if (PAIR && rank == 1)
+              mbar_arrive_remote(full_mma + 8u * s);
+            else
+              mbar_arrive(&full[s]);
+          }
           ++kc;
         }
       }
     }
   } else {
     // ------------------------------------------------ epilogue
+    // warp (q, half): TMEM lane quarter q, 32-column chunks c with c % 2 == half
     const int q = warp & 3;
+    const int half = (warp - PF_EPI0) >> 2;
     // the accumulator is released to the MMA thread's CTA (the even CTA of a pair)
     const uint32_t d_empty_mma = PAIR ? cluster_addr(smem_u32(d_empty), 0) : smem_u32(d_empty);
-    int ti = 0;
+    int nsub = 0;  // as the MMA thread: sub-tile number i is in slot i & 1
     int4 nxt = t0 < ntiles ? a.tiles[t0] : make_int4(0, 0, 0, 0);
-    for (int t = t0; t < ntiles; t += tstep, ++ti) {
+    for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
       const int4 tile = nxt;
       if (t + tstep < ntiles) nxt = a.tiles[t + tstep];
-      const int ab = ti & 1;
-      bool stop = *abort_flag != 0;
-      if (!stop && !mbar_wait(&d_full[ab], (ti >> 1) & 1, abort_flag)) {
-        *abort_flag = 1;
-        flag_status(a.status, DEV_TIMEOUT_MMA);
-        stop = true;
-      }
-      // the gate / up warp pair takes the same decision before its hand-offs
-      if (EPI == 1) stop = named_bar_or(6 + (q & 1), 64, stop);
-      if (stop) break;
-      tc_fence_after();
-      const uint32_t dbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + ab * PF_NMAX;
-      const int nchunk = (tile.w + 31) / 32;
-      for (int c = 0; c < nchunk; ++c) {
-        uint32_t r[32];
-        tmem_ld32(dbase + 32 * c, r);
-        tmem_ld_wait();
-        if (EPI == 1) {
-          const int pair = q & 1;
-          float* xb = xbuf + pair * 32 * 33;
-          if (q >= 2) {  // up rows: hand u to the gate warp of the same features
+      const PfSubTiles<PAIR> st(tile.w);
+      for (int hs = 0; hs < 2 && !*abort_flag; ++hs) {
+        if (st.n[hs] == 0) continue;
+        const int sl = nsub & 1;
+        if (!mbar_wait(&d_full[sl], (nsub >> 1) & 1, abort_flag)) {
+          *abort_flag = 1;
+          flag_status(a.status, DEV_TIMEOUT_MMA);
+          break;
+        }
+        ++nsub;
+        tc_fence_after();
+        const uint32_t dbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + sl * PF_SUBN;
+        const int row0 = tile.z + st.start[hs];   // sorted row of the slot's column 0
+        const int nrows = st.rows[hs];
+        const int nchunk = (nrows + 31) / 32;
+        for (int c = half; c < nchunk; c += 2) {
+          uint32_t r[32];
+          tmem_ld32(dbase + 32 * c, r);
+          tmem_ld_wait();
+          if constexpr (EPI == 1) {
+            // lane l: gate (bit 3 clear) or up row of feature f; partners l ^ 8 (up / gate of f) and
+            // l ^ 16 (feature f +- 16); a gate lane finishes even columns, an up lane odd ones
+            const bool up = (lane >> 3) & 1;
+            const int F = tile.y * 64 + pf_gu_feature(32 * q + lane);     // intermediate index
+            const int hcol = (F & ~31) + 2 * (F & 15);                      // H position of F (lanes < 16) and F + 16
 #pragma unroll
-            for (int i = 0; i < 32; ++i) xb[lane * 33 + i] = __uint_as_float(r[i]);
-            named_bar_sync(2 + pair, 64);
-            named_bar_sync(4 + pair, 64);
-          } else {
-            named_bar_sync(2 + pair, 64);
-            const int f = tile.y * 64 + 32 * q + lane;                   // intermediate index
-            const int col = (f & ~31) + ((f & 31) < 16 ? 2 * (f & 15) : 2 * (f & 15) + 1);
-            for (int i = 0; i < 32; ++i) {
-              const int p = 32 * c + i;
-              if (p < tile.w) {
-                const float g = __uint_as_float(r[i]);
-                const float u = xb[lane * 33 + i];
-                const float h = __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
-                a.Hs[static_cast<int64_t>(tile.z + p) * a.I + col] = __float2half_rn(h);
-              }
+            for (int i = 0; i < 16; ++i) {
+              const uint32_t send = up ? r[2 * i] : r[2 * i + 1];
+              const float other = __uint_as_float(__shfl_xor_sync(0xffffffffu, send, 8));
+              const float g = up ? other : __uint_as_float(r[2 * i]);
+              const float u = up ? __uint_as_float(r[2 * i + 1]) : other;
+              const float hv = __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
+              const uint32_t hb = __half_as_ushort(__float2half_rn(hv));
+              const uint32_t hp = __shfl_xor_sync(0xffffffffu, hb, 16);
+              const int p = 32 * c + 2 * i + (up ? 1 : 0);   // column of this lane's h
+              if (lane < 16 && p < nrows)
+                *reinterpret_cast<uint32_t*>(a.Hs + static_cast<int64_t>(row0 + p) * a.I + hcol) = hb | (hp << 16);
             }
-            named_bar_sync(4 + pair, 64);
-          }
-        } else if (EPI == 3) {
-          const int fo = tile.y * 128 + 32 * q + lane;   // output feature
-          for (int i = 0; i < 32; ++i)
-            if (32 * c + i < tile.w) a.out[static_cast<int64_t>(tile.z + 32 * c + i) * a.Hd + fo] = __uint_as_float(r[i]);
-        } else {
-          const int fo = tile.y * 128 + 32 * q + lane;   // output feature
-          const int pl = 32 * c + lane;
-          const int2 tw = pl < tile.w ? a.tokw[tile.z + pl] : make_int2(0, 0);
-          for (int i = 0; i < 32; ++i) {
-            const int tok = __shfl_sync(0xffffffffu, tw.x, i);
-            const float wt = __int_as_float(__shfl_sync(0xffffffffu, tw.y, i));
-            if (32 * c + i < tile.w) red_add_f32(a.out + static_cast<int64_t>(tok) * a.Hd + fo, wt * __uint_as_float(r[i]));
+          } else if constexpr (EPI == 3) {
+            const int fo = tile.y * 128 + 32 * q + lane;   // output feature
+            for (int i = 0; i < 32; ++i)
+              if (32 * c + i < nrows) a.out[static_cast<int64_t>(row0 + 32 * c + i) * a.Hd + fo] = __uint_as_float(r[i]);
+          } else {
+            const int fo = tile.y * 128 + 32 * q + lane;   // output feature
+            const int pl = 32 * c + lane;
+            const int2 tw = pl < nrows ? a.tokw[row0 + pl] : make_int2(0, 0);
+            for (int i = 0; i < 32; ++i) {
+              const int tok = __shfl_sync(0xffffffffu, tw.x, i);
+              const float wt = __int_as_float(__shfl_sync(0xffffffffu, tw.y, i));
+              if (32 * c + i < nrows) red_add_f32(a.out + static_cast<int64_t>(tok) * a.Hd + fo, wt * __uint_as_float(r[i]));
+            }
           }
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (PAIR)
-          mbar_arrive_remote(d_empty_mma + 8u * ab);
-        else
-          mbar_arrive(&d_empty[ab]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR)
+            mbar_arrive_remote(d_empty_mma + 8u * sl);
+          else
+            mbar_arrive(&d_empty[sl]);
+        }
       }
     }
   }
@@ -971,7 +1042,7 @@ cudaError_t launch_pf_gemm(PfKernel kern, int cl, size_t smem, cudaStream_t s, c
 // Workspace layout (offsets in bytes, each 256-aligned).
 void prefill_ws_layout(int T, int k, int E, int64_t hidden, int64_t inter, size_t* off) {
   const size_t n = static_cast<size_t>(T) * k;
-  const size_t tiles = n / PF_NMAX + E + 1;
+  const size_t tiles = n / PF_CAP_ONE + E + 1;   // token tiles of both tile caps fit
   const size_t segs = static_cast<size_t>(pf_nsegs(static_cast<int>(n)));
   size_t o = 0;
   off[0] = o; o = align_up(o + 4 * E + 4 * segs * E + 8 * E + 4, 256);  // counts, segment histograms, eoff, etb
@@ -1003,6 +1074,8 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   int* counts = reinterpret_cast<int*>(wsb + off[0]);
   int* order = reinterpret_cast<int*>(wsb + off[1]);
   int2* tokw = reinterpret_cast<int2*>(wsb + off[2]);
+  // CTA pairs share each MMA when both GEMMs have an even number of feature tiles
+  const int cl = (I / 64) % 2 == 0 && (H / 128) % 2 == 0 ? 2 : 1;
   PrefillTiles tl;
   tl.t1 = reinterpret_cast<int4*>(wsb + off[3]);
   tl.t2 = reinterpret_cast<int4*>(wsb + off[4]);
@@ -1010,12 +1083,14 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   tl.n2 = tl.n1 + 1;
   tl.F1 = I / 64;
   tl.F2 = H / 128;
+  // token tiles of at most 192 rows: one accumulator slot each, so the two
+  // slots double-buffer and the SwiGLU / combine epilogues of a tile run
+  // under the next tile's MMAs
+  tl.cap = PF_CAP_ONE;
   __half* xs = reinterpret_cast<__half*>(wsb + off[6]);
   __half* hs = reinterpret_cast<__half*>(wsb + off[7]);
   uint32_t* status = device_status_ptr();
 
-  // CTA pairs share each MMA when both GEMMs have an even number of feature tiles
-  const int cl = (I / 64) % 2 == 0 && (H / 128) % 2 == 0 ? 2 : 1;
   CUtensorMap m1, m2, q1, s1, q2, s2;
   if (!make_map(&m1, xs, n, H, pf_boxr_host(cl)) || !make_map(&m2, hs, n, I, pf_boxr_host(cl)) ||
       !make_weight_maps(&q1, &s1, gu) || !make_weight_maps(&q2, &s2, dn))
@@ -1030,7 +1105,7 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   int* etb = eoff + E;
   if (launch_pdl(prefill_scan_kernel, dim3(1), dim3(1024), 0, s, n, E, hist, counts, eoff, etb, tl) != cudaSuccess)
     return MOEX_ECUDA;
-  const int64_t max_tiles = (static_cast<int64_t>(n) / PF_NMAX + E + 1) * (tl.F1 + tl.F2);
+  const int64_t max_tiles = (static_cast<int64_t>(n) / PF_CAP_ONE + E + 1) * (tl.F1 + tl.F2);
   if (launch_pdl(prefill_tiles_kernel, dim3(static_cast<unsigned>((max_tiles + 255) / 256)), dim3(256), 0, s, E,
                  static_cast<const int*>(counts), static_cast<const int*>(eoff), static_cast<const int*>(etb),
                  tl) != cudaSuccess)
@@ -1082,7 +1157,7 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
 
 // Dense prefill workspace: tiles, totals, Xs.
 void dense_ws_layout(int T, int64_t rows, int64_t K, size_t* off) {
-  const size_t tiles = static_cast<size_t>(pf_token_tiles(T)) * static_cast<size_t>(rows / 128);
+  const size_t tiles = static_cast<size_t>(pf_token_tiles(T, PF_CAP_ONE)) * static_cast<size_t>(rows / 128);
   size_t o = 0;
   off[0] = o; o = align_up(o + 16 * tiles, 256);                     // tiles
   off[1] = o; o = align_up(o + 16, 256);                             // totals
@@ -1110,8 +1185,12 @@ moex_status launch_dense_prefill(const moex_qweight* W, const uint16_t* x, int T
   const int cl = F % 2 == 0 ? 2 : 1;
   CUtensorMap bm, qm, sm;
   if (!make_map(&bm, xs, T, K, pf_boxr_host(cl)) || !make_weight_maps(&qm, &sm, W)) return MOEX_ECUDA;
-  const int ntiles = pf_token_tiles(T) * F;
-  if (launch_pdl(dense_tiles_kernel, dim3((ntiles + 255) / 256), dim3(256), 0, s, T, F, tiles, n1) != cudaSuccess)
+  // a pair takes tiles of up to 384 tokens (two accumulator slots): each
+  // dequantised weight stage feeds twice the MMA work, and the plain-store
+  // epilogue is short enough to leave exposed
+  const int cap = cl == 2 ? PF_CAP_PAIR : PF_CAP_ONE;
+  const int ntiles = pf_token_tiles(T, cap) * F;
+  if (launch_pdl(dense_tiles_kernel, dim3((ntiles + 255) / 256), dim3(256), 0, s, T, F, cap, tiles, n1) != cudaSuccess)
     return MOEX_ECUDA;
   const int64_t gthreads = static_cast<int64_t>(T) * (K / QK);
   if (launch_pdl(prefill_gather_kernel, dim3(static_cast<unsigned>((gthreads + 255) / 256)), dim3(256), 0, s, x, K, 1,
