@@ -16,13 +16,28 @@ between the two products, the top-k outputs combined):
 
 Readings (pages silent): H is rounded to FP16 once from the exact value; the
 sort is stable by token, which does not change any result.
+
+The integer route of the same layer (``moe_prefill_q8``; #1525 Change: the
+prompt path's SwiGLU fused with the q8_1 quantisation of H, ``swiglu_quant``
+writing q8_1 rows for the down product, ``quantize_mmq_q8_1``) keeps the
+first product on FP16 operands and replaces the second:
+
+    H       = silu(g) * u                         FP32, no FP16 rounding
+    Hq, Hd  = q8_1(H)                             per 32-feature block
+    o       = sum_b fp32(dw[r,b]) * Hd[b] * I_b   the block-integer GEMV of gemv.py
+    out[t]  = sum_{k ascending} w[t, k] * o[(t, k)]
+
+Reading (pages silent): H reaches the quantiser as the FP32 value of
+silu(g) * u, exactly as the decode layer's H does.
 """
 from __future__ import annotations
 
 import numpy as np
 
 from . import formats
+from . import gemv as _gemv
 from . import moe as _moe
+from . import q8_1 as _q8_1
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
@@ -142,3 +157,63 @@ def moe_prefill(gate_up, down, x_bf16: np.ndarray, ids: np.ndarray, w: np.ndarra
             out[i] += float(w[t, s]) * O[i, s]
             out_A[i] += abs(float(w[t, s])) * O_A[i, s]
     return dict(tokens=tokens, out=out, out_A=out_A, g=G, u=U, H=Hs, gu_A=gu_A)
+
+
+def moe_prefill_q8(gate_up, down, x_bf16: np.ndarray, ids: np.ndarray, w: np.ndarray,
+                   tokens=None, fmt: str = "iq4_nl", h_override=None, down_fmt=None):
+    """The integer route of the prefill layer for ``tokens`` (default: every
+    token): the first product as in ``moe_prefill`` (FP16 operands, float64
+    sums), H = silu(g) * u taken to FP32, q8_1 of H per 32-feature block,
+    then the down product as block-integer dots (the GEMV of #1424 / #242)
+    and the top-k combine in slot order.
+
+    ``h_override(t, slot)`` may return an FP32 H row that replaces the
+    oracle's before its quantisation (the tests quantise the GPU's own H).
+
+    Returns dict: tokens, out [n, hidden] float64, out_A (error scale of the
+    combine), g, u, H (float64) [n, k, inter], Hq int8 [n, k, inter], Hd
+    float32 [n, k, inter/32], gu_A [n, k, 2*inter]."""
+    T, hidden = x_bf16.shape
+    k = ids.shape[1]
+    if tokens is None:
+        tokens = list(range(T))
+    Wgu = ExpertCache(fmt, gate_up)
+    inter = Wgu[int(ids[tokens[0], 0])].shape[0] // 2
+    n = len(tokens)
+    G = np.zeros((n, k, inter))
+    U = np.zeros((n, k, inter))
+    gu_A = np.zeros((n, k, 2 * inter))
+    Hq = np.zeros((n, k, inter), dtype=np.int8)
+    Hd = np.zeros((n, k, inter // 32), dtype=np.float32)
+    O = np.zeros((n, k, hidden))
+    O_A = np.zeros((n, k, hidden))
+    Xh = fp16_rn(bf16_bits_to_f32(x_bf16[np.asarray(tokens)])).astype(np.float64)
+    ent = {}
+    for i, t in enumerate(tokens):
+        for s in range(k):
+            ent.setdefault(int(ids[t, s]), []).append((i, s))
+    for e in sorted(ent):
+        ii = np.array([i for i, _ in ent[e]])
+        ss = np.array([s for _, s in ent[e]])
+        wg = Wgu[e]
+        gu = Xh[ii] @ wg.T
+        gu_A[ii, ss] = np.abs(Xh[ii]) @ np.abs(wg).T
+        G[ii, ss], U[ii, ss] = gu[:, :inter], gu[:, inter:]
+        if h_override is not None:
+            h32 = np.stack([np.asarray(h_override(tokens[i], s), dtype=np.float32) for i, s in ent[e]])
+        else:
+            h32 = (_moe.silu(gu[:, :inter]) * gu[:, inter:]).astype(np.float32)
+        q, d, _ = _q8_1.quantize_q8_1(h32)
+        Hq[ii, ss] = q
+        Hd[ii, ss] = d
+        y, A = _gemv.gemv(down_fmt or fmt, down[e], q, d)
+        O[ii, ss] = y
+        O_A[ii, ss] = A
+    out = np.zeros((n, hidden))
+    out_A = np.zeros((n, hidden))
+    for i, t in enumerate(tokens):
+        for s in range(k):
+            out[i] += float(w[t, s]) * O[i, s]
+            out_A[i] += abs(float(w[t, s])) * O_A[i, s]
+    H = _moe.silu(G) * U
+    return dict(tokens=tokens, out=out, out_A=out_A, g=G, u=U, H=H, Hq=Hq, Hd=Hd, gu_A=gu_A)

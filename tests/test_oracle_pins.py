@@ -470,6 +470,77 @@ def test_prefill_brute_force_tiny():
         assert np.allclose(r["out"][t], out, rtol=1e-12, atol=1e-12)
 
 
+def _iq4_row_ints(blocks, row, kv):
+    """Codebook integers and exact scales of one IQ4_NL row, decoded by hand
+    from the block bytes (low nibble of byte j: element j, high: j + 16)."""
+    ints, scales = [], []
+    for blk in blocks[row]:
+        b = bytes(blk)
+        scales.append(_fp16_exact(b[0] | (b[1] << 8)))
+        lo = [kv[v & 15] for v in b[2:18]]
+        hi = [kv[v >> 4] for v in b[2:18]]
+        ints.append(lo + hi)
+    return ints, scales
+
+
+def test_prefill_q8_brute_force_tiny():
+    """The integer route redone by hand: g, u from the FP16 weights and
+    tokens in plain floats, H rounded to FP32 by struct, q8_1 with exact
+    rationals, the down product as integer block dots with exact scales."""
+    hidden, inter, k = 64, 64, 2
+    gu = [synth.expert_blocks("gate_up", e, hidden, inter, "iq4_nl", seed=43) for e in range(3)]
+    dn = [synth.expert_blocks("down", e, hidden, inter, "iq4_nl", seed=43) for e in range(3)]
+    xb = synth.bf16_activations(synth.rng(44), 2, hidden)
+    ids = np.array([[1, 2], [0, 1]])
+    w = np.array([[0.625, 0.375], [0.5, 0.5]])
+    kv = read_codebook()
+
+    def fp16w(blocks, row, col):
+        blk = bytes(blocks[row, col // 32])
+        d = _fp16_exact(blk[0] | (blk[1] << 8))
+        byte = blk[2 + (col % 32) % 16]
+        q = kv[(byte & 15) if (col % 32) < 16 else (byte >> 4)]
+        return struct.unpack("<e", struct.pack("<e", float(d * q)))[0]
+
+    H32, H64 = {}, {}
+    for t in range(2):
+        xs = [struct.unpack("<e", struct.pack("<e", struct.unpack("<f", struct.pack("<I", int(b) << 16))[0]))[0]
+              for b in xb[t]]
+        for s in range(k):
+            e = ids[t, s]
+            gg = [sum(fp16w(gu[e], i, c) * xs[c] for c in range(hidden)) for i in range(inter)]
+            uu = [sum(fp16w(gu[e], inter + i, c) * xs[c] for c in range(hidden)) for i in range(inter)]
+            H64[t, s] = [a / (1 + math.exp(-a)) * b for a, b in zip(gg, uu)]
+            H32[t, s] = [_f32(Fraction(v)) for v in H64[t, s]]
+    own = prefill.moe_prefill_q8(gu, dn, xb, ids, w)
+    for (t, s), h in H64.items():
+        assert np.allclose(own["H"][t, s], h, rtol=1e-9, atol=1e-12)
+    r = prefill.moe_prefill_q8(gu, dn, xb, ids, w, h_override=lambda t, s: np.array(H32[t, s], np.float32))
+    for t in range(2):
+        out = [Fraction(0)] * hidden
+        for s in range(k):
+            h = H32[t, s]
+            qs, ds = [], []
+            for b in range(inter // 32):
+                blk = h[32 * b:32 * b + 32]
+                amax = max(abs(v) for v in blk)
+                dd = _f32(Fraction(amax) / 127) if amax else 0.0
+                q = [_roundf(Fraction(_f32(Fraction(v) / Fraction(dd)))) if amax else 0 for v in blk]
+                qs += q
+                ds.append(dd)
+            assert r["Hq"][t, s].tolist() == qs and r["Hd"][t, s].tolist() == ds
+            wints, wsc = _iq4_row_ints(dn[ids[t, s]], 0, kv)  # shape check on row 0
+            assert len(wints) == inter // 32
+            for o in range(hidden):
+                wints, wsc = _iq4_row_ints(dn[ids[t, s]], o, kv)
+                acc = Fraction(0)
+                for b in range(inter // 32):
+                    I = sum(wq * xq for wq, xq in zip(wints[b], qs[32 * b:32 * b + 32]))
+                    acc += Fraction(_f32(wsc[b])) * Fraction(ds[b]) * I
+                out[o] += Fraction(w[t, s]) * acc
+        assert np.allclose(r["out"][t], [float(v) for v in out], rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------- mutations
 
 def test_planted_nibble_swap_is_caught(monkeypatch):
@@ -490,6 +561,13 @@ def test_planted_round_half_even_is_caught(monkeypatch):
     monkeypatch.setattr(q8_1, "round_half_away", lambda r: np.round(r.astype(np.float64)))
     with pytest.raises(AssertionError):
         test_q8_1_hand_fixture(read_q8_1_cases()[0])
+
+
+def test_planted_dropped_scale_in_prefill_q8_is_caught(monkeypatch):
+    orig = gemv.gemv_planes
+    monkeypatch.setattr(gemv, "gemv_planes", lambda dw, wq, dx, xq: orig(dw, wq, np.ones_like(dx), xq))
+    with pytest.raises(AssertionError):
+        test_prefill_q8_brute_force_tiny()
 
 
 def test_planted_dropped_scale_is_caught(monkeypatch):
