@@ -295,7 +295,7 @@ def decode_layer_detail(reps, copies=3):
             "weight_bytes": wbytes, "weight_GBps": round(wbytes / (t2 / reps) / 1e9, 1)}
 
 
-def prefill_layer_detail(reps=5, peak_tflops=None, T=8192, E=128):
+def prefill_layer_detail(reps=5, peak_tflops=None, T=8192, E=128, route="fp16"):
     """Grouped MoE prefill layer: T tokens x top-8 of E IQ4_NL experts,
     hidden 2560, inter 1536 (route + sort + gather + two tcgen05 GEMMs).
     The workload is 8192 tokens over 128 experts; 4096 over 64 keeps the
@@ -313,11 +313,17 @@ def prefill_layer_detail(reps=5, peak_tflops=None, T=8192, E=128):
     ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, k), dtype=torch.float32, device="cuda")
     out = torch.empty((T, hidden), dtype=torch.float32, device="cuda")
-    ws = torch.empty(mx.moe_prefill_workspace_bytes(T, k, E, hidden, inter), dtype=torch.uint8, device="cuda")
+    if route == "int8":
+        ws = torch.empty(mx.moe_prefill_q8_workspace_bytes(T, k, E, hidden, inter), dtype=torch.uint8, device="cuda")
+    else:
+        ws = torch.empty(mx.moe_prefill_workspace_bytes(T, k, E, hidden, inter), dtype=torch.uint8, device="cuda")
 
     def layer():
         mx.route_topk(logits, k, ids, w)
-        mx.moe_prefill(gu, dn, x, ids, w, out, ws)
+        if route == "int8":
+            mx.moe_prefill_q8(gu, dn, x, ids, w, out, ws)
+        else:
+            mx.moe_prefill(gu, dn, x, ids, w, out, ws)
     for _ in range(2):
         layer()
     torch.cuda.synchronize()
@@ -329,7 +335,7 @@ def prefill_layer_detail(reps=5, peak_tflops=None, T=8192, E=128):
     torch.cuda.synchronize()
     t = e0.elapsed_time(e1) * 1e-3 / reps
     flops = 2.0 * T * k * (2 * inter * hidden + hidden * inter)
-    d = {"tokens": T, "experts": E, "top_k": k, "layer_ms": round(t * 1e3, 3),
+    d = {"route": route, "tokens": T, "experts": E, "top_k": k, "layer_ms": round(t * 1e3, 3),
          "algorithmic_tflop": round(flops / 1e12, 4), "layer_tflops": round(flops / t / 1e12, 1)}
     if peak_tflops:
         d["frac_of_fp16_dense_peak"] = round(flops / t / 1e12 / peak_tflops, 3)
@@ -499,6 +505,8 @@ def run_ours(args, ws, rank, local):
         detail["moe_decode_20_experts"] = decode_layer_detail(500)
         torch.cuda.empty_cache()
         detail["moe_prefill_8192_tokens"] = prefill_layer_detail(5, peak_fp16())
+        torch.cuda.empty_cache()
+        detail["moe_prefill_int8_route_8192_tokens"] = prefill_layer_detail(3, None, route="int8")
         torch.cuda.empty_cache()
         detail["dense_prefill_iq4_nl_12288x2560_8192_tokens"] = dense_prefill_detail(10, peak_fp16())
 
@@ -711,6 +719,10 @@ def run_only(args):
         d = prefill_layer_detail(max(1, args.steps), peak_fp16(), args.pf_tokens, args.pf_experts)
         print(json.dumps({"only": "prefill", **d}))
         return
+    elif args.only == "prefill_q8":
+        d = prefill_layer_detail(max(1, args.steps), None, args.pf_tokens, args.pf_experts, route="int8")
+        print(json.dumps({"only": "prefill_q8", **d}))
+        return
     elif args.only == "dense_prefill":
         print(json.dumps({"only": "dense_prefill", **dense_prefill_detail(max(1, args.steps), peak_fp16())}))
         return
@@ -733,7 +745,7 @@ def run_only(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--only", default=None, help="profile helper: gemv_q8_0 | gemv_iq4_nl | decode | prefill | dense_prefill")
+    ap.add_argument("--only", default=None, help="profile helper: gemv_q8_0 | gemv_iq4_nl | decode | prefill | prefill_q8 | dense_prefill")
     ap.add_argument("--ncols", type=int, default=1)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)

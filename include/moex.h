@@ -251,6 +251,48 @@ moex_status moex_moe_prefill(const moex_qweight* gate_up, const moex_qweight* do
                              const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,
                              moex_stream stream);
 
+/* Workspace bytes of moex_moe_prefill_q8 for T tokens, top-k, E experts. */
+size_t moex_moe_prefill_q8_workspace_bytes(int T, int k, int E, int64_t hidden, int64_t inter);
+
+/*
+ * Byte offsets of the integer-route workspace: offsets[0] counts (then the
+ * sort's histograms and expert offsets), [1] order int32[T*k], [2] {token,
+ * weight bits} int32x2[T*k], [3] first-product tile list, [4] down-product
+ * tile list, [5] totals, [6] Xs FP16 [T*k][hidden] (interleaved blocks as in
+ * the FP16 route), [7] Hq int8 [T*k][inter] (natural order), [8] {d, s}
+ * float32x2 [T*k][inter/32], [9] total.  Rows are in sorted order (order[]).
+ */
+moex_status moex_moe_prefill_q8_workspace_layout(int T, int k, int E, int64_t hidden, int64_t inter,
+                                                 size_t* offsets);
+
+/*
+ * The grouped MoE prefill layer on its integer route (#1525 Change: the
+ * prompt path's SwiGLU fused with the q8_1 quantisation of H --
+ * swiglu_quant writing q8_1 rows -- and the down product as block-integer
+ * dots, the "MMQ" route beside the FP16 one):
+ *   g, u   = Wh_gu[e] . Xs   on FP16 tensor cores (tcgen05), as moex_moe_prefill
+ *   H      = silu(g) * u      (FP32, never rounded to FP16)
+ *   Hq, Hd = q8_1(H)          per 32-feature block, in the first product's epilogue
+ *   o      = sum_b fp32(dw[r,b]) * Hd[b] * (sum_i qw[r,32b+i] * Hq[32b+i])   (dp4a)
+ *   out[t] = sum_k w[t,k] * o[(t,k)]   (FP32 atomic adds: order not fixed)
+ * Arguments as moex_moe_prefill (no residual form); ws of
+ * moex_moe_prefill_q8_workspace_bytes() bytes.  Eight launches (sort:
+ * histogram, scan, two tile lists, scatter; gather, which also clears out;
+ * the tcgen05 first product; the dp4a down product).
+ */
+moex_status moex_moe_prefill_q8(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16, int T,
+                                const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,
+                                moex_stream stream);
+
+/*
+ * moex_moe_prefill_q8 that also writes H, for staged checking:
+ *   h_dbg : device FP32 [T*k][inter] in sorted-row order (16-byte aligned),
+ *           the values the q8_1 quantiser received.
+ */
+moex_status moex_moe_prefill_q8_debug(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16,
+                                      int T, const int32_t* ids, const float* w, int k, float* out, void* ws,
+                                      size_t ws_bytes, float* h_dbg, moex_stream stream);
+
 /* Workspace bytes of moex_dense_prefill for T tokens and a rows x K matrix. */
 size_t moex_dense_prefill_workspace_bytes(int T, int64_t rows, int64_t K);
 

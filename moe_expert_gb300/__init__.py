@@ -65,6 +65,12 @@ SIGNATURES = {
                                                          ctypes.POINTER(_SZ)]),
     "moex_moe_prefill": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _SZ, _P]),
     "moex_moe_decode_noalloc": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P]),
+    "moex_moe_prefill_q8_workspace_bytes": (_SZ, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _I64, _I64]),
+    "moex_moe_prefill_q8_workspace_layout": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _I64, _I64,
+                                                            ctypes.POINTER(_SZ)]),
+    "moex_moe_prefill_q8": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _SZ, _P]),
+    "moex_moe_prefill_q8_debug": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _SZ, _P,
+                                                 _P]),
     "moex_dense_prefill_workspace_bytes": (_SZ, [ctypes.c_int, _I64, _I64]),
     "moex_dense_prefill": (ctypes.c_int, [_QWP, _P, ctypes.c_int, _P, _I64, _P, _SZ, _P]),
     "moex_moe_decode_residual": (ctypes.c_int, [_QWP, _QWP, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _P, _SZ,
@@ -321,6 +327,41 @@ def moe_prefill(gate_up: PackedWeight, down: PackedWeight, x_bf16, ids, w, out=N
     _check(lib().moex_moe_prefill(ctypes.byref(gate_up.struct), ctypes.byref(down.struct), _ptr(x_bf16), T,
                                   _ptr(ids), _ptr(w), k, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
            "moex_moe_prefill")
+    return out
+
+
+def moe_prefill_q8_workspace_bytes(T: int, k: int, E: int, hidden: int, inter: int) -> int:
+    return int(lib().moex_moe_prefill_q8_workspace_bytes(T, k, E, hidden, inter))
+
+
+def moe_prefill_q8_workspace_layout(T: int, k: int, E: int, hidden: int, inter: int):
+    """Byte offsets of the integer-route workspace parts (see include/moex.h)."""
+    off = (ctypes.c_size_t * 10)()
+    _check(lib().moex_moe_prefill_q8_workspace_layout(T, k, E, hidden, inter, off),
+           "moex_moe_prefill_q8_workspace_layout")
+    return [int(v) for v in off]
+
+
+def moe_prefill_q8(gate_up: PackedWeight, down: PackedWeight, x_bf16, ids, w, out=None, ws=None, h_dbg=None,
+                   stream=None):
+    """The grouped MoE prefill layer on its integer route (q8_1 rows of H, a
+    block-integer down product).  Arguments as moe_prefill; with h_dbg (FP32
+    [T*k, inter]) the layer also writes H in sorted-row order."""
+    torch = _torch()
+    T, hidden = x_bf16.shape
+    k = ids.shape[1]
+    E, inter = gate_up.n_mats, down.K
+    if out is None:
+        out = torch.empty((T, hidden), dtype=torch.float32, device=x_bf16.device)
+    if ws is None:
+        ws = torch.empty(moe_prefill_q8_workspace_bytes(T, k, E, hidden, inter), dtype=torch.uint8,
+                         device=x_bf16.device)
+    args = (ctypes.byref(gate_up.struct), ctypes.byref(down.struct), _ptr(x_bf16), T, _ptr(ids), _ptr(w), k,
+            _ptr(out), _ptr(ws), ws.numel())
+    if h_dbg is None:
+        _check(lib().moex_moe_prefill_q8(*args, _stream(stream)), "moex_moe_prefill_q8")
+    else:
+        _check(lib().moex_moe_prefill_q8_debug(*args, _ptr(h_dbg), _stream(stream)), "moex_moe_prefill_q8_debug")
     return out
 
 

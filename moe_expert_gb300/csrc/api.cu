@@ -288,6 +288,49 @@ moex_status moex_dense_prefill(const moex_qweight* W, const uint16_t* x_bf16, in
   return launch_dense_prefill(W, x_bf16, T, y, ldy, ws, stream);
 }
 
+size_t moex_moe_prefill_q8_workspace_bytes(int T, int k, int E, int64_t hidden, int64_t inter) {
+  if (T < 1 || k < 1 || E < 1 || hidden < 128 || inter < 64) return 0;
+  return moe_prefill_q8_ws_bytes(T, k, E, hidden, inter);
+}
+
+moex_status moex_moe_prefill_q8_workspace_layout(int T, int k, int E, int64_t hidden, int64_t inter,
+                                                 size_t* offsets) {
+  if (!offsets || T < 1 || k < 1 || E < 1 || hidden < 128 || inter < 64) return MOEX_EINVAL;
+  prefill_q8_ws_layout(T, k, E, hidden, inter, offsets);
+  return MOEX_OK;
+}
+
+static moex_status prefill_q8_checked(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16,
+                                      int T, const int32_t* ids, const float* w, int k, float* out, void* ws,
+                                      size_t ws_bytes, float* h_dbg, moex_stream stream) {
+  moex_status st = check_weight(gate_up);
+  if (st != MOEX_OK) return st;
+  st = check_weight(down);
+  if (st != MOEX_OK) return st;
+  if (!x_bf16 || !ids || !w || !out || !ws) return MOEX_EINVAL;
+  if (T < 1 || k < 1 || k > 16 || static_cast<int64_t>(T) * k > (int64_t(1) << 26)) return MOEX_EINVAL;
+  if (gate_up->n_mats != down->n_mats || gate_up->n_mats > 4096) return MOEX_EINVAL;
+  if (gate_up->rows % 2 != 0 || down->rows != gate_up->K || down->K != gate_up->rows / 2) return MOEX_EINVAL;
+  if (gate_up->K % 128 != 0 || down->K % 64 != 0) return MOEX_EUNSUPPORTED;
+  if (static_cast<int64_t>(gate_up->n_mats) * gate_up->rows > INT32_MAX) return MOEX_EUNSUPPORTED;
+  if (ws_bytes < moe_prefill_q8_ws_bytes(T, k, gate_up->n_mats, gate_up->K, down->K)) return MOEX_ENOSPACE;
+  if (!aligned16(x_bf16) || !aligned16(ws) || !aligned16(out)) return MOEX_EALIGN;
+  if (h_dbg && !aligned16(h_dbg)) return MOEX_EALIGN;
+  return launch_moe_prefill_q8(gate_up, down, x_bf16, T, ids, w, k, out, ws, h_dbg, stream);
+}
+
+moex_status moex_moe_prefill_q8(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16, int T,
+                                const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,
+                                moex_stream stream) {
+  return prefill_q8_checked(gate_up, down, x_bf16, T, ids, w, k, out, ws, ws_bytes, nullptr, stream);
+}
+
+moex_status moex_moe_prefill_q8_debug(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16,
+                                      int T, const int32_t* ids, const float* w, int k, float* out, void* ws,
+                                      size_t ws_bytes, float* h_dbg, moex_stream stream) {
+  return prefill_q8_checked(gate_up, down, x_bf16, T, ids, w, k, out, ws, ws_bytes, h_dbg, stream);
+}
+
 moex_status moex_moe_prefill(const moex_qweight* gate_up, const moex_qweight* down, const uint16_t* x_bf16, int T,
                              const int32_t* ids, const float* w, int k, float* out, void* ws, size_t ws_bytes,
                              moex_stream stream) {

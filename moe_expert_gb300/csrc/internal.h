@@ -66,6 +66,12 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
                                const int32_t* ids, const float* w, int k, const float* residual, float* out, void* ws,
                                cudaStream_t s);
 
+size_t moe_prefill_q8_ws_bytes(int T, int k, int E, int64_t hidden, int64_t inter);
+void prefill_q8_ws_layout(int T, int k, int E, int64_t hidden, int64_t inter, size_t* off);
+moex_status launch_moe_prefill_q8(const moex_qweight* gu, const moex_qweight* dn, const uint16_t* x, int T,
+                                  const int32_t* ids, const float* w, int k, float* out, void* ws, float* h_dbg,
+                                  cudaStream_t s);
+
 size_t dense_prefill_ws_bytes(int T, int64_t rows, int64_t K);
 moex_status launch_dense_prefill(const moex_qweight* W, const uint16_t* x, int T, float* y, int64_t ldy, void* ws,
                                  cudaStream_t s);

@@ -339,6 +339,9 @@ struct GemmArgs {
   const int4* tiles;
   const int* ntiles;
   __half* Hs;          // GEMM 1 output [rows][I] (interleaved blocks)
+  int8_t* Hq;          // integer route: q8_1 quants of H [rows][I] (natural order)
+  float2* Hds;         // integer route: {d, s} of each 32-feature block [rows][I/32]
+  float* Hf;           // integer route, optional: FP32 H [rows][I] (natural order)
   int I;
   float* out;          // GEMM 2 output [T][Hd]
   int Hd;
@@ -424,14 +427,27 @@ __device__ __forceinline__ void red_add_f32(float* p, float v) {
 }
 
 
+// Named barrier over `count` threads that also ORs a flag across them, so
+// every participant takes the same branch afterwards.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool flag) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(out)
+      : "r"(static_cast<uint32_t>(flag)), "r"(id), "r"(count)
+      : "memory");
+  return out != 0;
+}
+
 struct PfSmem {
-  int b, raw, bars, tmem, abort_flag, total;
+  int b, raw, bars, xch, tmem, abort_flag, total;
   __host__ __device__ PfSmem() {
     int o = 0;
     b = o; o += PF_NB_ST * PF_STAGE_B;                          // 1024-aligned (dynamic smem base)
     raw = o; o += PF_NR_ST * PF_RAW_STAGE;                      // 1024-aligned
     bars = o; o += 8 * (2 * PF_NB_ST + 2 * PF_NA_ST + 2 * PF_NR_ST + 4 + 1);
     o = (o + 15) & ~15;
+    xch = o; o += 4 * 2 * 2 * 32 * 4;                          // integer route: per warp pair, amax and sums of 32 columns
     tmem = o; o += 16;
     abort_flag = o; o += 16;
     total = o + 1024;                                          // slack for aligning the base
@@ -492,6 +508,8 @@ __device__ __forceinline__ int pf_gu_raw_row(int m) {
 
 // EPI == 1: SwiGLU -> H (FP16).  EPI == 2: weighted combine into out.
 // EPI == 3: dense product, out[token][feature] = D (FP32, stride Hd).
+// EPI == 4: SwiGLU -> FP32 H -> q8_1 of each 32-feature block (the integer
+// route's first product; Hq, Hds, and H itself when Hf is given).
 // WF: the weight format, IQ4_NL (raw stages of 4 k-steps) or Q8_0 (2).
 // PAIR: CTA pairs (clusters of two) on neighbouring feature tiles of the same
 // token tile share M = 256 MMAs (tcgen05 cta_group::2): each CTA dequantises
@@ -531,6 +549,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.tmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
   constexpr int BOXR = pf_boxr<PAIR>();
+  constexpr bool GU = EPI == 1 || EPI == 4;  // GEMM 1: gate and up rows of 64 features
+  float* xch = reinterpret_cast<float*>(smem + L.xch);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -735,8 +755,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
         if (t + tstep < ntiles) nxt = a.tiles[t + tstep];  // read one tile ahead
         const int64_t base = static_cast<int64_t>(tile.x) * a.rows_per_expert;
         // weight rows of raw rows 0..63 and 64..127: gate and up features (GEMM 1) or 128 outputs (GEMM 2)
-        const int y0 = static_cast<int>(EPI == 1 ? base + tile.y * 64 : base + tile.y * 128);
-        const int y1 = static_cast<int>(EPI == 1 ? base + a.I + tile.y * 64 : base + tile.y * 128 + 64);
+        const int y0 = static_cast<int>(GU ? base + tile.y * 64 : base + tile.y * 128);
+        const int y1 = static_cast<int>(GU ? base + a.I + tile.y * 64 : base + tile.y * 128 + 64);
         for (int g = 0; g < ngroups; ++g, ++rc) {
           const int r = rc % PF_NR_ST;
           if (rc >= PF_NR_ST && !mbar_wait(&r_empty[r], ((rc / PF_NR_ST) - 1) & 1, abort_flag)) {
@@ -766,7 +786,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
     const int q = warp & 3;
     const int h = (warp - PF_DQ0) >> 2;
     const int m = 32 * q + lane;                          // A row = TMEM lane
-    const int rr = EPI == 1 ? pf_gu_raw_row(m) : m;       // its row in the raw stage
+    const int rr = GU ? pf_gu_raw_row(m) : m;             // its row in the raw stage
     // raw stage rows: 128 bytes, 16-byte chunk c stored at chunk c ^ (row & 7)
     const int qoff = (rr >> 6) * 64 * 128 + (rr & 63) * 128;
     const int soff = PF_RAW_QS + (rr >> 6) * 64 * 16 + (rr & 63) * 16;
@@ -845,11 +865,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
       for (int hs = 0; hs < 2 && !*abort_flag; ++hs) {
         if (st.n[hs] == 0) continue;
         const int sl = nsub & 1;
-        if (!mbar_wait(&d_full[sl], (nsub >> 1) & 1, abort_flag)) {
+        bool stop = !mbar_wait(&d_full[sl], (nsub >> 1) & 1, abort_flag);
+        if (stop) {
           *abort_flag = 1;
           flag_status(a.status, DEV_TIMEOUT_MMA);
-          break;
         }
+        // (integer route) the two warps of a feature block exchange through
+        // shared memory: both take the same decision before the hand-offs
+        if constexpr (EPI == 4) stop = named_bar_or(2 + (q >> 1) + 2 * half, 64, stop);
+        if (stop) break;
         ++nsub;
         tc_fence_after();
         const uint32_t dbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + sl * PF_SUBN;
@@ -878,6 +902,69 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
               const int p = 32 * c + 2 * i + (up ? 1 : 0);   // column of this lane's h
               if (lane < 16 && p < nrows)
                 *reinterpret_cast<uint32_t*>(a.Hs + static_cast<int64_t>(row0 + p) * a.I + hcol) = hb | (hp << 16);
+            }
+          } else if constexpr (EPI == 4) {
+            // as EPI 1 (lane l: gate or up row of feature F, a gate lane finishing
+            // the even columns, an up lane the odd ones); a q8_1 block of H is the
+            // 32 features of warps q and q ^ 1: amax and the sum of the quants are
+            // reduced over the 16 lanes of a column in each warp, then exchanged
+            const bool up = (lane >> 3) & 1;
+            const int F = tile.y * 64 + pf_gu_feature(32 * q + lane);     // intermediate index
+            const int bar_id = 2 + (q >> 1) + 2 * half;
+            float* mine = xch + ((q >> 1) + 2 * half) * 128 + (q & 1) * 32;   // [amax | sums] x 32 columns
+            const float* theirs = xch + ((q >> 1) + 2 * half) * 128 + ((q & 1) ^ 1) * 32;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {   // columns 16 hf .. 16 hf + 15 (pairs i = 8 hf .. 8 hf + 7)
+              float hv[8], mx[8];
+#pragma unroll
+              for (int ii = 0; ii < 8; ++ii) {
+                const int i = 8 * hf + ii;
+                const uint32_t send = up ? r[2 * i] : r[2 * i + 1];
+                const float other = __uint_as_float(__shfl_xor_sync(0xffffffffu, send, 8));
+                const float g = up ? other : __uint_as_float(r[2 * i]);
+                const float u = up ? __uint_as_float(r[2 * i + 1]) : other;
+                hv[ii] = __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
+                float m_ = fabsf(hv[ii]);
+                m_ = fmaxf(m_, __shfl_xor_sync(0xffffffffu, m_, 1));
+                m_ = fmaxf(m_, __shfl_xor_sync(0xffffffffu, m_, 2));
+                m_ = fmaxf(m_, __shfl_xor_sync(0xffffffffu, m_, 4));
+                mx[ii] = fmaxf(m_, __shfl_xor_sync(0xffffffffu, m_, 16));
+              }
+              if ((lane & 0x17) == 0)
+#pragma unroll
+                for (int ii = 0; ii < 8; ++ii) mine[2 * (8 * hf + ii) + (up ? 1 : 0)] = mx[ii];
+              named_bar_sync(bar_id, 64);
+              int qv[8], sm[8];
+              float dv[8];
+#pragma unroll
+              for (int ii = 0; ii < 8; ++ii) {
+                const float amax = fmaxf(mx[ii], theirs[2 * (8 * hf + ii) + (up ? 1 : 0)]);
+                dv[ii] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
+                qv[ii] = amax > 0.f ? static_cast<int>(roundf(__fdiv_rn(hv[ii], dv[ii]))) : 0;
+                int s_ = qv[ii];
+                s_ += __shfl_xor_sync(0xffffffffu, s_, 1);
+                s_ += __shfl_xor_sync(0xffffffffu, s_, 2);
+                s_ += __shfl_xor_sync(0xffffffffu, s_, 4);
+                sm[ii] = s_ + __shfl_xor_sync(0xffffffffu, s_, 16);
+              }
+              if ((lane & 0x17) == 0)
+#pragma unroll
+                for (int ii = 0; ii < 8; ++ii) mine[64 + 2 * (8 * hf + ii) + (up ? 1 : 0)] = __int_as_float(sm[ii]);
+              named_bar_sync(bar_id, 64);
+#pragma unroll
+              for (int ii = 0; ii < 8; ++ii) {
+                const int col = 2 * (8 * hf + ii) + (up ? 1 : 0);
+                const int p = 32 * c + col;   // column of this lane's h
+                if (p < nrows) {
+                  const int64_t row = row0 + p;
+                  a.Hq[row * a.I + F] = static_cast<int8_t>(qv[ii]);
+                  if (a.Hf) a.Hf[row * a.I + F] = hv[ii];
+                  if ((q & 1) == 0 && (lane & 0x17) == 0) {
+                    const int total = sm[ii] + __float_as_int(theirs[64 + col]);
+                    a.Hds[row * (a.I / QK) + (F >> 5)] = make_float2(dv[ii], __fmul_rn(dv[ii], static_cast<float>(total)));
+                  }
+                }
+              }
             }
           } else if constexpr (EPI == 3) {
             const int fo = tile.y * 128 + 32 * q + lane;   // output feature
@@ -914,6 +1001,210 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
       tmem_dealloc_pair(tmem, 512);
     else
       tmem_dealloc(tmem, 512);
+  }
+}
+
+// ----------------------------------------------------------------- integer route: down product
+
+// The down product of the integer route (#1525 Change: q8_1 rows of H for the
+// down product, the integer "MMQ" route): for a tile of 128 output features
+// of one expert and up to 64 of its sorted rows,
+//   o[f][p] = sum_b fp32(dw[f,b]) * d_h[p,b] * I[f,p,b],
+//   I = sum_{i<32} qw[f,32b+i] * qh[p,32b+i]       (int32, dp4a chains)
+// summed over the blocks b in order, then out[token(p)] += w * o (atomic).
+// Each weight block is decoded once per tile into shared memory (IQ4_NL to
+// the int8 byte order of iq4nl_lookup4, with H's words permuted to match)
+// and applied to the tile's 64 rows; the next block's bytes are loaded into
+// registers while the current one is multiplied.
+constexpr int QD_ROWS = 128;     // output features per tile
+constexpr int QD_TOK = 64;       // sorted rows per tile
+constexpr int QD_THREADS = 256;  // warp w: rows 8w .. 8w+7, lane l: features l + 32j
+
+struct Q8DownArgs {
+  const uint8_t* qs;
+  const uint8_t* sc;
+  int qrow, scrow;
+  int64_t rows_per_expert;
+  int I;                 // inputs of the down product (multiple of 32)
+  const int4* tiles;     // {expert, feature tile, first sorted row, rows}
+  const int* ntiles;
+  const int8_t* hq;      // [rows][I]
+  const float2* hds;     // [rows][I/32] {d, s}
+  const int2* tokw;      // per sorted row: token, weight bits
+  float* out;            // [T][Hd], accumulated
+  int Hd;
+};
+
+// Tile list of the integer down product: thread i of one 1024-thread CTA
+// owns experts 4i .. 4i+3; each expert's rows are cut into balanced token
+// tiles of at most 64 rows, each paired with every feature tile.
+__global__ void __launch_bounds__(1024) q8_tiles_kernel(int E, int F, const int* __restrict__ counts,
+                                                        const int* __restrict__ eoff, int4* __restrict__ tiles,
+                                                        int* __restrict__ ntiles) {
+  __shared__ int red[32];
+  pdl_wait();
+  pdl_launch_dependents();
+  int nt[4];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = 4 * threadIdx.x + i;
+    nt[i] = e < E ? pf_token_tiles(counts[e], QD_TOK) : 0;
+    sum += nt[i];
+  }
+  int base = sum;
+  const int total = block_exscan(base, red);
+  if (threadIdx.x == 0) *ntiles = total * F;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = 4 * threadIdx.x + i;
+    for (int tt = 0; tt < nt[i]; ++tt) {
+      int r0, rows;
+      pf_tile_span(counts[e], QD_TOK, tt, &r0, &rows);
+      for (int f = 0; f < F; ++f) tiles[static_cast<int64_t>(base + tt) * F + f] = make_int4(e, f, eoff[e] + r0, rows);
+    }
+    base += nt[i];
+  }
+}
+
+__device__ __forceinline__ uint4 ldg_nc16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(QD_THREADS) q8_down_kernel(Q8DownArgs a) {
+  // decoded weight words of 128 rows (the two 16-byte halves of row r swapped
+  // when bit 2 of r is set, so a quarter warp's 16-byte reads of 8 rows hit
+  // 32 distinct banks) and H's words of 64 rows, double-buffered by block
+  __shared__ __align__(16) uint32_t wsm[2][QD_ROWS * 8];
+  __shared__ float wdm[2][QD_ROWS];
+  __shared__ __align__(16) uint32_t xsm[2][QD_TOK * 8];
+  __shared__ float xdm[2][QD_TOK];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int ntiles = *a.ntiles;
+  const int NB = a.I / QK;
+  for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int4 tile = a.tiles[t];
+    const int64_t wrow0 = static_cast<int64_t>(tile.x) * a.rows_per_expert + static_cast<int64_t>(tile.y) * QD_ROWS;
+    // loaders: thread f < 128 fetches weight row f, thread 128 + p fetches H row p
+    uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
+    uint32_t sw = 0;
+    float xd = 0.f;
+    auto fetch = [&](int b) {
+      if (tid < QD_ROWS) {
+        const uint8_t* src = a.qs + (wrow0 + tid) * a.qrow + b * FmtTraits<FMT>::QBYTES;
+        q0 = ldg_nc16(src);
+        if (FMT == MOEX_Q8_0) q1 = ldg_nc16(src + 16);
+        sw = *reinterpret_cast<const uint16_t*>(a.sc + (wrow0 + tid) * a.scrow + 2 * b);
+      } else if (tid < QD_ROWS + QD_TOK) {
+        const int p = tid - QD_ROWS;
+        if (p < tile.w) {
+          const int8_t* src = a.hq + static_cast<int64_t>(tile.z + p) * a.I + b * QK;
+          q0 = *reinterpret_cast<const uint4*>(src);
+          q1 = *reinterpret_cast<const uint4*>(src + 16);
+          xd = a.hds[static_cast<int64_t>(tile.z + p) * NB + b].x;
+        } else {
+          q0 = q1 = make_uint4(0, 0, 0, 0);
+          xd = 0.f;
+        }
+      }
+    };
+    auto stage = [&](int buf) {
+      if (tid < QD_ROWS) {
+        uint32_t wv[8];
+        if constexpr (FMT == MOEX_Q8_0) {
+          wv[0] = q0.x; wv[1] = q0.y; wv[2] = q0.z; wv[3] = q0.w;
+          wv[4] = q1.x; wv[5] = q1.y; wv[6] = q1.z; wv[7] = q1.w;
+        } else {
+          const uint32_t W[4] = {q0.x, q0.y, q0.z, q0.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t fl = W[i] ^ 0x88888888u;
+            wv[2 * i] = iq4nl_lookup4(W[i], fl);
+            wv[2 * i + 1] = iq4nl_lookup4(W[i] >> 16, fl >> 16);
+          }
+        }
+        const int sx = (tid >> 2) & 1;
+        uint4* dst = reinterpret_cast<uint4*>(&wsm[buf][tid * 8]);
+        dst[sx] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        dst[sx ^ 1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+        wdm[buf][tid] = __half2float(__ushort_as_half(static_cast<uint16_t>(sw)));
+      } else if (tid < QD_ROWS + QD_TOK) {
+        const int p = tid - QD_ROWS;
+        uint32_t xv[8];
+        const uint32_t X[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        if constexpr (FMT == MOEX_Q8_0) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) xv[i] = X[i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            xv[2 * i] = prmt(X[i], X[i + 4], 0x5140);
+            xv[2 * i + 1] = prmt(X[i], X[i + 4], 0x7362);
+          }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(&xsm[buf][p * 8]);
+        dst[0] = make_uint4(xv[0], xv[1], xv[2], xv[3]);
+        dst[1] = make_uint4(xv[4], xv[5], xv[6], xv[7]);
+        xdm[buf][p] = xd;
+      }
+    };
+    fetch(0);
+    stage(0);
+    __syncthreads();
+    float acc[4][8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[j][i] = 0.f;
+    for (int b = 0; b < NB; ++b) {
+      const int buf = b & 1;
+      if (b + 1 < NB) fetch(b + 1);
+      uint32_t wv[4][8];
+      float dw[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = lane + 32 * j;
+        const int sx = (r >> 2) & 1;
+        const uint4* src = reinterpret_cast<const uint4*>(&wsm[buf][r * 8]);
+        const uint4 lo = src[sx], hi = src[sx ^ 1];
+        wv[j][0] = lo.x; wv[j][1] = lo.y; wv[j][2] = lo.z; wv[j][3] = lo.w;
+        wv[j][4] = hi.x; wv[j][5] = hi.y; wv[j][6] = hi.z; wv[j][7] = hi.w;
+        dw[j] = wdm[buf][r];
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int p = 8 * warp + i;
+        const uint4* src = reinterpret_cast<const uint4*>(&xsm[buf][p * 8]);
+        const uint4 lo = src[0], hi = src[1];
+        const uint32_t xv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        const float dx = xdm[buf][p];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          int I = 0;
+#pragma unroll
+          for (int z = 0; z < 8; ++z) I = dp4a(wv[j][z], xv[z], I);
+          acc[j][i] = __fadd_rn(acc[j][i], __fmul_rn(__int2float_rn(I), __fmul_rn(dw[j], dx)));
+        }
+      }
+      if (b + 1 < NB) stage(buf ^ 1);
+      __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int p = 8 * warp + i;
+      if (p < tile.w) {
+        const int2 tw = a.tokw[tile.z + p];
+        const float wt = __int_as_float(tw.y);
+        float* dst = a.out + static_cast<int64_t>(tw.x) * a.Hd + tile.y * QD_ROWS + lane;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) red_add_f32(dst + 32 * j, wt * acc[j][i]);
+      }
+    }
   }
 }
 
@@ -1153,6 +1444,125 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   g2.status = status;
   if (launch_pf_gemm(k2, cl, L.total, s, m2, q2, s2, g2) != cudaSuccess) return MOEX_ECUDA;
   return MOEX_OK;
+}
+
+// Integer-route workspace: the sort (as the FP16 route), the GEMM 1 tile
+// list, the down product's tile list (64-row token tiles), totals, Xs, and
+// H as q8_1 rows (quants, then {d, s} per block).
+void prefill_q8_ws_layout(int T, int k, int E, int64_t hidden, int64_t inter, size_t* off) {
+  const size_t n = static_cast<size_t>(T) * k;
+  const size_t segs = static_cast<size_t>(pf_nsegs(static_cast<int>(n)));
+  size_t o = 0;
+  off[0] = o; o = align_up(o + 4 * E + 4 * segs * E + 8 * E + 4, 256);
+  off[1] = o; o = align_up(o + 4 * n, 256);
+  off[2] = o; o = align_up(o + 8 * n, 256);
+  off[3] = o; o = align_up(o + 16 * (n / PF_CAP_ONE + E + 1) * (inter / 64), 256);
+  off[4] = o; o = align_up(o + 16 * (n / QD_TOK + E + 1) * (hidden / QD_ROWS), 256);
+  off[5] = o; o = align_up(o + 32, 256);                                  // totals (GEMM 1 ..., down tiles at [4])
+  off[6] = o; o = align_up(o + 2 * n * hidden, 256);                      // Xs
+  off[7] = o; o = align_up(o + n * inter, 256);                           // Hq
+  off[8] = o; o = align_up(o + 8 * n * (inter / QK), 256);                // {d, s}
+  off[9] = o;
+}
+
+size_t moe_prefill_q8_ws_bytes(int T, int k, int E, int64_t hidden, int64_t inter) {
+  size_t off[10];
+  prefill_q8_ws_layout(T, k, E, hidden, inter, off);
+  return off[9];
+}
+
+moex_status launch_moe_prefill_q8(const moex_qweight* gu, const moex_qweight* dn, const uint16_t* x, int T,
+                                  const int32_t* ids, const float* w, int k, float* out, void* ws, float* h_dbg,
+                                  cudaStream_t s) {
+  const int E = gu->n_mats;
+  const int H = static_cast<int>(gu->K), I = static_cast<int>(dn->K);
+  const int n = T * k;
+  size_t off[10];
+  prefill_q8_ws_layout(T, k, E, H, I, off);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  int* counts = reinterpret_cast<int*>(wsb + off[0]);
+  int* order = reinterpret_cast<int*>(wsb + off[1]);
+  int2* tokw = reinterpret_cast<int2*>(wsb + off[2]);
+  const int cl = (I / 64) % 2 == 0 ? 2 : 1;
+  PrefillTiles tl;
+  tl.t1 = reinterpret_cast<int4*>(wsb + off[3]);
+  tl.t2 = tl.t1;                     // no tcgen05 GEMM 2 in this route: its list is left empty
+  tl.n1 = reinterpret_cast<int*>(wsb + off[5]);
+  tl.n2 = tl.n1 + 1;
+  tl.F1 = I / 64;
+  tl.F2 = 0;
+  tl.cap = PF_CAP_ONE;
+  int4* qt = reinterpret_cast<int4*>(wsb + off[4]);
+  int* nq = tl.n1 + 4;
+  __half* xs = reinterpret_cast<__half*>(wsb + off[6]);
+  int8_t* hq = reinterpret_cast<int8_t*>(wsb + off[7]);
+  float2* hds = reinterpret_cast<float2*>(wsb + off[8]);
+  uint32_t* status = device_status_ptr();
+
+  CUtensorMap m1, q1, s1;
+  if (!make_map(&m1, xs, n, H, pf_boxr_host(cl)) || !make_weight_maps(&q1, &s1, gu)) return MOEX_ECUDA;
+  int* hist = counts + E;
+  const int S = pf_nsegs(n);
+  const size_t esm = static_cast<size_t>(E) * sizeof(int);
+  if (launch_pdl(prefill_hist_kernel, dim3(S), dim3(256), esm, s, ids, n, E, hist, status) != cudaSuccess)
+    return MOEX_ECUDA;
+  int* eoff = hist + static_cast<int64_t>(S) * E;
+  int* etb = eoff + E;
+  if (launch_pdl(prefill_scan_kernel, dim3(1), dim3(1024), 0, s, n, E, hist, counts, eoff, etb, tl) != cudaSuccess)
+    return MOEX_ECUDA;
+  const int64_t max_tiles = (static_cast<int64_t>(n) / PF_CAP_ONE + E + 1) * tl.F1;
+  if (launch_pdl(prefill_tiles_kernel, dim3(static_cast<unsigned>((max_tiles + 255) / 256)), dim3(256), 0, s, E,
+                 static_cast<const int*>(counts), static_cast<const int*>(eoff), static_cast<const int*>(etb),
+                 tl) != cudaSuccess)
+    return MOEX_ECUDA;
+  if (launch_pdl(q8_tiles_kernel, dim3(1), dim3(1024), 0, s, E, H / QD_ROWS, static_cast<const int*>(counts),
+                 static_cast<const int*>(eoff), qt, nq) != cudaSuccess)
+    return MOEX_ECUDA;
+  if (launch_pdl(prefill_scatter_kernel, dim3(S), dim3(32), esm, s, ids, w, n, k, E, static_cast<const int*>(hist),
+                 order, tokw) != cudaSuccess)
+    return MOEX_ECUDA;
+  const int64_t gthreads = static_cast<int64_t>(n) * (H / QK);
+  if (launch_pdl(prefill_gather_kernel, dim3(static_cast<unsigned>((gthreads + 255) / 256)), dim3(256), 0, s, x, H,
+                 k, static_cast<const int*>(tl.n1 + 2), static_cast<const int*>(order), xs,
+                 static_cast<const float4*>(nullptr), reinterpret_cast<float4*>(out),
+                 static_cast<int64_t>(T) * H / 4) != cudaSuccess)
+    return MOEX_ECUDA;
+  const PfSmem L;
+  const PfKernel k1 = pf_kernel<4>(cl, gu->fmt);
+  if (ensure_smem(reinterpret_cast<const void*>(k1), L.total) != cudaSuccess) return MOEX_ECUDA;
+  GemmArgs g1 = {};
+  g1.qs = static_cast<const uint8_t*>(gu->qs);
+  g1.sc = static_cast<const uint8_t*>(gu->scales);
+  g1.qrow = static_cast<int>(qs_row_bytes(gu->fmt, gu->K));
+  g1.scrow = static_cast<int>(sc_row_bytes(gu->K));
+  g1.rows_per_expert = gu->rows;
+  g1.K = H;
+  g1.tiles = tl.t1;
+  g1.ntiles = tl.n1;
+  g1.Hq = hq;
+  g1.Hds = hds;
+  g1.Hf = h_dbg;
+  g1.I = I;
+  g1.status = status;
+  if (launch_pf_gemm(k1, cl, L.total, s, m1, q1, s1, g1) != cudaSuccess) return MOEX_ECUDA;
+  Q8DownArgs d = {};
+  d.qs = static_cast<const uint8_t*>(dn->qs);
+  d.sc = static_cast<const uint8_t*>(dn->scales);
+  d.qrow = static_cast<int>(qs_row_bytes(dn->fmt, dn->K));
+  d.scrow = static_cast<int>(sc_row_bytes(dn->K));
+  d.rows_per_expert = dn->rows;
+  d.I = I;
+  d.tiles = qt;
+  d.ntiles = nq;
+  d.hq = hq;
+  d.hds = hds;
+  d.tokw = tokw;
+  d.out = out;
+  d.Hd = H;
+  auto kd = dn->fmt == MOEX_Q8_0 ? q8_down_kernel<MOEX_Q8_0> : q8_down_kernel<MOEX_IQ4_NL>;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kd, QD_THREADS, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
+  return cuda_status(launch_pdl(kd, dim3(sm_count() * per_sm), dim3(QD_THREADS), 0, s, d));
 }
 
 // Dense prefill workspace: tiles, totals, Xs.

@@ -155,6 +155,45 @@ def test_prefill_and_dense_validation():
     assert dp(x=odd) == 2
 
 
+def test_prefill_q8_validation():
+    """The integer-route prefill rejects bad arguments on the host, in the
+    order its checks run, before anything is enqueued."""
+    import moe_expert_gb300 as mx
+    L = ensure_lib()
+    null = ctypes.c_void_p(0)
+    buf = ctypes.create_string_buffer(4096 + 16)
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    p = ctypes.c_void_p(base)
+    odd = ctypes.c_void_p(base + 4)
+    E, H, I, T, k = 4, 256, 128, 8, 2
+    gu = mx.QWeight(2, E, 2 * I, H, base, base)
+    dn = mx.QWeight(2, E, H, I, base, base)
+    need = L.moex_moe_prefill_q8_workspace_bytes(T, k, E, H, I)
+    assert need > 0 and L.moex_moe_prefill_q8_workspace_bytes(T, k, E, H, 32) == 0
+    off = mx.moe_prefill_q8_workspace_layout(T, k, E, H, I)
+    assert off[9] == need and all(off[i] <= off[i + 1] and off[i] % 256 == 0 for i in range(9))
+    assert off[8] - off[7] >= T * k * I and off[9] - off[8] >= 8 * T * k * (I // 32)
+    big = 1 << 40
+
+    def pf(g=gu, d=dn, x=p, t=T, kk=k, out=p, ws=p, nbytes=big, h=None):
+        if h is None:
+            return L.moex_moe_prefill_q8(ctypes.byref(g), ctypes.byref(d), x, t, p, p, kk, out, ws, nbytes, null)
+        return L.moex_moe_prefill_q8_debug(ctypes.byref(g), ctypes.byref(d), x, t, p, p, kk, out, ws, nbytes, h,
+                                           null)
+
+    assert pf(x=null) == 1
+    assert pf(t=0) == 1
+    assert pf(kk=17) == 1
+    assert pf(d=mx.QWeight(2, E + 1, H, I, base, base)) == 1            # expert counts differ
+    assert pf(d=mx.QWeight(2, E, H, 2 * I, base, base)) == 1            # down K != inter
+    assert pf(g=mx.QWeight(2, E, 2 * I, 96, base, base),
+              d=mx.QWeight(2, E, 96, I, base, base)) == 3               # hidden not a multiple of 128
+    assert pf(nbytes=need - 1) == 7
+    assert pf(x=odd) == 2
+    assert pf(out=odd) == 2
+    assert pf(h=odd) == 2                                               # H output misaligned
+
+
 def test_decode_residual_validation():
     import moe_expert_gb300 as mx
     L = ensure_lib()
