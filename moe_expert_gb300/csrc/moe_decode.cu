@@ -412,7 +412,7 @@ struct DnSmem {
     bars = o; o += 16 * nst;
     cnt = o; o += 4 * nst;
     abort_flag = o; o += 16;
-    ids = o; o += 8 * MAX_ENTRIES;
+    ids = o; o += 12 * MAX_ENTRIES;   // ids, build_groups scratch, routing weights
     o = (o + 15) & ~15;
     groups = o; o += static_cast<int>(sizeof(Groups));
     o = (o + 15) & ~15;
@@ -514,7 +514,11 @@ __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
   }
   // The routing ids were complete before the gate/up kernel let this grid
   // launch, so they are read before griddepcontrol.wait.
-  for (int j = threadIdx.x; j < a.n; j += blockDim.x) ids_s[j] = a.ids[j];
+  float* w_s = reinterpret_cast<float*>(ids_s + 2 * MAX_ENTRIES);  // routing weights, for the combine
+  for (int j = threadIdx.x; j < a.n; j += blockDim.x) {
+    ids_s[j] = a.ids[j];
+    w_s[j] = a.w[j];
+  }
   __syncthreads();
   build_groups(G, ids_s, a.n, a.E, nullptr, ids_s + MAX_ENTRIES);
   MOEX_TRACE_STAMP(0);
@@ -589,7 +593,7 @@ __global__ void __launch_bounds__(MAXT, 1) moe_dn_kernel(DecodeArgs a) {
       const float* pr = osum + (j * rows_max + rl) * NS;
       float o = pr[0];
       for (int ks = 1; ks < NS; ++ks) o = o + pr[ks];   // slice order, as the dense GEMV
-      acc = __fadd_rn(acc, __fmul_rn(a.w[j], o));
+      acc = __fadd_rn(acc, __fmul_rn(w_s[j], o));
     }
     const int64_t o = static_cast<int64_t>(t) * a.H + row_begin + rl;
     a.out[o] = a.residual ? __fadd_rn(a.residual[o], acc) : acc;
