@@ -61,6 +61,19 @@ int max_smem_optin() {
   return g_smem[d];
 }
 
+EncodeTiledFn encode_tiled_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
 cudaError_t ensure_smem(const void* func, size_t bytes) {
   // The attribute is per function and device; it is raised once to the
   // largest size seen, so calls captured into a CUDA graph after a first

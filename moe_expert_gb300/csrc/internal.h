@@ -1,6 +1,7 @@
 // Host-side declarations shared by the moex translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -36,6 +37,13 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 // Raises the dynamic shared-memory limit of a kernel once per device.
 cudaError_t ensure_smem(const void* func, size_t bytes);
+
+// The driver's cuTensorMapEncodeTiled (looked up once through the runtime's
+// entry-point query, so no link against libcuda), or nullptr.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
 
 inline moex_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOEX_OK : MOEX_ECUDA; }
 

@@ -1212,26 +1212,10 @@ __global__ void __launch_bounds__(QD_THREADS) q8_down_kernel(Q8DownArgs a) {
 
 namespace {
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
 // 2-D FP16 map over [rows][cols] (row pitch cols*2 bytes), box 64 inputs x
 // boxr rows, 128-byte swizzle.
 bool make_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int boxr) {
-  EncodeTiledFn fn = encode_fn();
+  EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
@@ -1246,7 +1230,7 @@ bool make_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int boxr) 
 // box box_x bytes x 64 rows.
 bool make_plane_map(CUtensorMap* m, const void* base, int64_t rows, int64_t used, int64_t pitch, int box_x,
                     CUtensorMapSwizzle swz) {
-  EncodeTiledFn fn = encode_fn();
+  EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(used), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch)};

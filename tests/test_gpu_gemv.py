@@ -66,11 +66,15 @@ def test_block_dots_bit_exact(fmt):
     assert np.array_equal(dots.astype(np.int64), og.block_dots(wq, rq))
 
 
-@pytest.mark.parametrize("fmt,K", [("q8_0", 2560), ("iq4_nl", 2560), ("iq4_nl", 1536), ("q8_0", 96)])
-def test_columns_bitwise_equal_single_column_calls(fmt, K):
+@pytest.mark.parametrize("fmt,rows,K", [("q8_0", 129, 2560), ("iq4_nl", 129, 2560), ("iq4_nl", 129, 1536),
+                                         ("q8_0", 129, 96),
+                                         # more than one round of 16-row tiles a CTA, ragged last round
+                                         ("q8_0", 10500, 2560), ("iq4_nl", 13001, 2560), ("q8_0", 60001, 480)])
+def test_columns_bitwise_equal_single_column_calls(fmt, rows, K):
     import torch
     import moe_expert_gb300 as mx
-    W, xq, xds, y, ref, A, _, _ = _run(fmt, 129, K, 8, seed=9)
+    W, xq, xds, y, ref, A, _, _ = _run(fmt, rows, K, 8, seed=9)
+    assert_within(y, ref, A, f"{fmt} {rows}x{K} c8")
     for c in range(8):
         y1 = to_np(mx.qgemv(W, xq[c:c + 1].contiguous(), xds[c:c + 1].contiguous()))
         assert np.array_equal(y1[0].view(np.uint32), y[c].view(np.uint32)), c
