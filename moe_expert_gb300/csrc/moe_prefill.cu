@@ -18,7 +18,7 @@
 // with tcgen05.st (one thread per row, no shared-memory round trip); the
 // sorted token rows are the B operand, boxes of a 2-D TMA tensor map with the
 // 128-byte swizzle; tcgen05.mma (K = 16, N = tile tokens rounded up) into a
-// double-buffered FP32 accumulator in TMEM, read back by four epilogue warps
+// double-buffered FP32 accumulator in TMEM, read back by eight epilogue warps
 // with tcgen05.ld.  Because the token count of an expert is the MMA's N,
 // ragged experts cost a few padded columns per tile instead of a partial
 // 128-row M tile.  CTAs run in pairs (clusters of two) on neighbouring
