@@ -44,12 +44,17 @@ namespace moex {
 constexpr int PF_SUBN = 192;     // tokens of one MMA sub-tile (one TMEM accumulator slot)
 constexpr int PF_CAP_PAIR = 384; // tokens of a tile for CTA pairs: two sub-tiles
 constexpr int PF_CAP_ONE = 192;  // tokens of a tile for single CTAs: one sub-tile
-constexpr int PF_BK = 64;        // inputs per k-step (one 128-byte swizzle row of FP16)
-constexpr int PF_NB_ST = 4;      // B (token) stages in shared memory
-constexpr int PF_NA_ST = 4;      // A (weight) stages in TMEM
-constexpr int PF_STAGE_B = 192 * PF_BK * 2;       // bytes of one B stage: at most 192 token rows a CTA
-static_assert(PF_NB_ST == PF_NA_ST, "A and B stages advance together");
+constexpr int PF_BK = 128;       // inputs per k-step (two 128-byte swizzle rows of FP16); K's last may be 64
+constexpr int PF_BOXK = 64;      // inputs per token-row TMA box (one 128-byte swizzle row)
+constexpr int PF_NB_ST = 3;      // B (token) stages in shared memory
+constexpr int PF_NA_ST = 2;      // A (weight) stages in TMEM
+constexpr int PF_KD = 6;         // k-step-done barriers: k-step kc's MMAs commit to kdone[kc % 6]
+static_assert(PF_KD % PF_NB_ST == 0 && PF_KD % PF_NA_ST == 0, "a k-step's stages free on its own barrier");
+constexpr int PF_HALF_B = 192 * PF_BOXK * 2;      // bytes of one 64-input half of a B stage: at most 192 token rows a CTA
+constexpr int PF_STAGE_B = 2 * PF_HALF_B;         // bytes of one B stage
 constexpr int PF_ACOL = 2 * PF_SUBN;              // first TMEM column of the A stages (after two slots)
+constexpr int PF_ACOLS = PF_BK / 2;               // TMEM columns of one A stage (FP16 pairs)
+static_assert(PF_ACOL + PF_NA_ST * PF_ACOLS <= 512, "accumulators and A stages fit the TMEM");
 constexpr int PF_DQ_WARPS = 8;   // dequantising warps: two per TMEM lane quarter, one IQ4_NL block each
 constexpr int PF_DQ0 = 3;        // first dequantising warp
 constexpr int PF_EPI0 = PF_DQ0 + PF_DQ_WARPS;           // first epilogue warp
@@ -58,11 +63,11 @@ constexpr int PF_THREADS = (PF_EPI0 + PF_EPI_WARPS) * 32;  // warp 0 B TMA, 1 MM
 // Raw weight stages: the IQ4_NL bytes of 128 rows x 4 k-steps (8 blocks a
 // row), two boxes of 64 rows x 128 bytes with the 128-byte swizzle, then
 // their FP16 scales, two boxes of 64 rows x 16 bytes.
-constexpr int PF_RAW_KS = 4;                      // k-steps per IQ4_NL raw stage (Q8_0: 2, same bytes)
+constexpr int PF_RAW_KS = 2;                      // k-steps per IQ4_NL raw stage (Q8_0: 1, same bytes)
 constexpr int PF_NR_ST = 4;                       // raw stages
 constexpr int PF_RAW_QS = 128 * 128;              // nibble bytes of a raw stage
 constexpr int PF_RAW_STAGE = PF_RAW_QS + 128 * 16;  // + scale bytes (multiple of 1024)
-__host__ __device__ constexpr int pf_raw_ks(int wf) { return wf == MOEX_Q8_0 ? 2 : PF_RAW_KS; }
+__host__ __device__ constexpr int pf_raw_ks(int wf) { return wf == MOEX_Q8_0 ? 1 : PF_RAW_KS; }
 
 // ----------------------------------------------------------------- sort
 
@@ -445,7 +450,7 @@ struct PfSmem {
     int o = 0;
     b = o; o += PF_NB_ST * PF_STAGE_B;                          // 1024-aligned (dynamic smem base)
     raw = o; o += PF_NR_ST * PF_RAW_STAGE;                      // 1024-aligned
-    bars = o; o += 8 * (2 * PF_NB_ST + 2 * PF_NA_ST + 2 * PF_NR_ST + 4 + 1);
+    bars = o; o += 8 * (2 * PF_NB_ST + PF_KD + PF_NA_ST + 2 * PF_NR_ST + 4 + 1);
     o = (o + 15) & ~15;
     xch = o; o += 4 * 2 * 2 * 32 * 4;                          // integer route: per warp pair, amax and sums of 32 columns
     tmem = o; o += 16;
@@ -532,16 +537,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   uint8_t* sb = smem + L.b;
   uint8_t* sraw = smem + L.raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* b_full = bars;
-  // k-step kc uses A stage and B stage kc % PF_NA_ST; one MMA commit per
-  // k-step releases both (for a pair, in both CTAs)
-  uint64_t* ab_empty = b_full + PF_NB_ST;
+  // k-step kc uses B stage kc % PF_NB_ST and A stage kc % PF_NA_ST; its one
+  // MMA commit (for a pair, to both CTAs) completes kdone[kc % PF_KD], which
+  // frees both stages
+  uint64_t* b_full = bars;                  // this CTA's B stage has landed
+  uint64_t* b_peer = b_full + PF_NB_ST;     // (issuing CTA of a pair) the odd CTA's B stage has landed
+  uint64_t* kdone = b_peer + PF_NB_ST;
   // full[s] (on the CTA that issues the MMAs): the A stage is in TMEM in
   // every CTA of the pair (each dequantising warp arrives; the odd CTA's
-  // remotely) and the odd CTA's B stage is in place (its forwarder arrives);
-  // the issuing CTA's own B stage is b_full[s]
-  uint64_t* full = ab_empty + PF_NB_ST;
-  uint64_t* d_full = full + 2 * PF_NA_ST;   // accumulator slot h holds a finished sub-tile
+  // remotely)
+  uint64_t* full = kdone + PF_KD;
+  uint64_t* d_full = full + PF_NA_ST;       // accumulator slot h holds a finished sub-tile
   uint64_t* d_empty = d_full + 2;           // accumulator slot h has been read by every epilogue warp
   uint64_t* done_bar = d_empty + 2;
   uint64_t* r_full = done_bar + 1;
@@ -556,9 +562,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   if (threadIdx.x == 0) {
     for (int i = 0; i < PF_NB_ST; ++i) {
       mbar_init(&b_full[i], 1);
-      mbar_init(&ab_empty[i], 1);   // the MMA thread's commit
+      mbar_init(&b_peer[i], 1);     // the odd CTA's forwarder
     }
-    for (int i = 0; i < PF_NA_ST; ++i) mbar_init(&full[i], PAIR ? 2 * PF_DQ_WARPS + 1 : PF_DQ_WARPS);
+    for (int i = 0; i < PF_KD; ++i) mbar_init(&kdone[i], 1);  // the MMA thread's commit
+    for (int i = 0; i < PF_NA_ST; ++i) mbar_init(&full[i], PAIR ? 2 * PF_DQ_WARPS : PF_DQ_WARPS);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&d_full[i], 1);
       mbar_init(&d_empty[i], (PAIR ? 2 : 1) * PF_EPI_WARPS);  // every epilogue warp (of both CTAs of a pair)
@@ -597,7 +604,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   const int t0 = PAIR ? 2 * (blockIdx.x >> 1) + rank : blockIdx.x;
   const int tstep = PAIR ? 2 * (gridDim.x >> 1) : gridDim.x;
   const int ntiles = *a.ntiles;
-  const int KS = a.K / PF_BK;
+  const int KS = (a.K + PF_BK - 1) / PF_BK;   // k-steps; the last takes one half when K % 128 == 64
+  const bool half_last = (a.K % PF_BK) != 0;
 
   if (warp == 0) {
     // ------------------------------------------------ B producer (TMA of this CTA's token rows)
@@ -611,20 +619,23 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
         int src[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) src[h] = tile.z + st.start[h] + (PAIR ? rank * (st.n[h] / 2) : 0);
-        const uint32_t bytes = (st.nbox[0] + st.nbox[1]) * BOXR * PF_BK * 2;
+        const uint32_t half_bytes = (st.nbox[0] + st.nbox[1]) * BOXR * PF_BOXK * 2;
         for (int ks = 0; ks < KS; ++ks, ++kc) {
           const int s = kc % PF_NB_ST;
-          if (kc >= PF_NB_ST && !mbar_wait(&ab_empty[s], ((kc / PF_NB_ST) - 1) & 1, abort_flag)) {
+          const int j0 = kc - PF_NB_ST;  // the k-step that used this stage before
+          if (j0 >= 0 && !mbar_wait(&kdone[j0 % PF_KD], (j0 / PF_KD) & 1, abort_flag)) {
             *abort_flag = 1;
             flag_status(a.status, DEV_TIMEOUT_MMA);
             break;
           }
-          mbar_arrive_expect_tx(&b_full[s], bytes);
+          const int nhalf = (half_last && ks == KS - 1) ? 1 : 2;
+          mbar_arrive_expect_tx(&b_full[s], nhalf * half_bytes);
+          for (int j = 0; j < nhalf; ++j)
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            for (int bx = 0; bx < st.nbox[h]; ++bx)
-              tma_load_2d(sb + s * PF_STAGE_B + (st.off[h] + bx * BOXR) * PF_BK * 2, &bmap, ks * PF_BK,
-                          src[h] + BOXR * bx, &b_full[s]);
+            for (int h = 0; h < 2; ++h)
+              for (int bx = 0; bx < st.nbox[h]; ++bx)
+                tma_load_2d(sb + s * PF_STAGE_B + j * PF_HALF_B + (st.off[h] + bx * BOXR) * PF_BOXK * 2, &bmap,
+                            ks * PF_BK + j * PF_BOXK, src[h] + BOXR * bx, &b_full[s]);
         }
       }
       // after an abort, let the copies already issued land before the CTA exits
@@ -639,7 +650,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
     // the even CTA, whose MMA reads it (the A stage is announced by the
     // dequantising warps themselves)
     if (lane == 0) {
-      const uint32_t peer_full = cluster_addr(smem_u32(full), 0);
+      const uint32_t peer_b = cluster_addr(smem_u32(b_peer), 0);
       int kc = 0;
       for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
         for (int ks = 0; ks < KS; ++ks, ++kc) {
@@ -649,16 +660,16 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
             flag_status(a.status, DEV_TIMEOUT_MMA);
             break;
           }
-          mbar_arrive_remote(peer_full + 8u * s);
+          mbar_arrive_remote(peer_b + 8u * s);
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (one CTA, or the even CTA of a pair)
     if (lane == 0) {
-      uint32_t ab_empty_peer = 0, d_full_peer = 0;
+      uint32_t kdone_peer = 0, d_full_peer = 0;
       if constexpr (PAIR) {
-        ab_empty_peer = cluster_addr(smem_u32(ab_empty), 1);
+        kdone_peer = cluster_addr(smem_u32(kdone), 1);
         d_full_peer = cluster_addr(smem_u32(d_full), 1);
       }
       int kc = 0;
@@ -681,7 +692,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
           sub[h] = nsub + h;
           idesc[h] = idesc_f16_f32(PAIR ? 256 : 128, st.n[h] > 0 ? st.n[h] : 16);
           dcol[h] = tmem + (sub[h] & 1) * PF_SUBN;
-          bdesc[h] = smem_desc_sw128(smem_u32(sb) + st.off[h] * PF_BK * 2);
+          bdesc[h] = smem_desc_sw128(smem_u32(sb) + st.off[h] * PF_BOXK * 2);
         }
         // the slots' previous sub-tiles must have been read out first
         bool ok = true;
@@ -693,31 +704,34 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
           break;
         }
         for (int ks = 0; ks < KS; ++ks, ++kc) {
-          const int s = kc % PF_NA_ST;
-          if (!mbar_wait(&b_full[s], (kc / PF_NB_ST) & 1, abort_flag) ||
-              !mbar_wait(&full[s], (kc / PF_NA_ST) & 1, abort_flag)) {
+          const int sb_ = kc % PF_NB_ST, sa = kc % PF_NA_ST;
+          if (!mbar_wait(&b_full[sb_], (kc / PF_NB_ST) & 1, abort_flag) ||
+              (PAIR && !mbar_wait(&b_peer[sb_], (kc / PF_NB_ST) & 1, abort_flag)) ||
+              !mbar_wait(&full[sa], (kc / PF_NA_ST) & 1, abort_flag)) {
             *abort_flag = 1;
             flag_status(a.status, DEV_TIMEOUT_MMA);
             break;
           }
           tc_fence_after();
-          const uint32_t acol = tmem + PF_ACOL + s * 32;
-          const uint64_t boff = static_cast<uint64_t>((s * PF_STAGE_B) >> 4);
+          const uint32_t acol = tmem + PF_ACOL + sa * PF_ACOLS;
+          const uint64_t boff = static_cast<uint64_t>((sb_ * PF_STAGE_B) >> 4);
+          const int nkk = (half_last && ks == KS - 1) ? PF_BOXK / 16 : PF_BK / 16;
           for (int h = 0; h < nh; ++h) {
-#pragma unroll
-            for (int kk = 0; kk < PF_BK / 16; ++kk) {
+            for (int kk = 0; kk < nkk; ++kk) {
+              // 16-input step kk: half kk / 4 of the stage, 32 bytes further per step within it
+              const uint64_t bd = bdesc[h] + boff + (kk >> 2) * (PF_HALF_B >> 4) + 2 * (kk & 3);
               if constexpr (PAIR)
-                mma_f16_ts_pair(dcol[h], acol + kk * 8, bdesc[h] + boff + 2 * kk, idesc[h], (ks | kk) != 0);
+                mma_f16_ts_pair(dcol[h], acol + kk * 8, bd, idesc[h], (ks | kk) != 0);
               else
-                mma_f16_ts(dcol[h], acol + kk * 8, bdesc[h] + boff + 2 * kk, idesc[h], (ks | kk) != 0);
+                mma_f16_ts(dcol[h], acol + kk * 8, bd, idesc[h], (ks | kk) != 0);
             }
           }
           issued_any = true;
           if constexpr (PAIR) {
-            mma_commit_pair(smem_u32(&ab_empty[s]));
-            mma_commit_pair(ab_empty_peer + 8u * s);
+            mma_commit_pair(smem_u32(&kdone[kc % PF_KD]));
+            mma_commit_pair(kdone_peer + 8u * (kc % PF_KD));
           } else {
-            mma_commit(&ab_empty[s]);
+            mma_commit(&kdone[kc % PF_KD]);
           }
         }
         if (*abort_flag) break;
@@ -781,8 +795,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
     }
   } else if (warp < PF_EPI0) {
     // ------------------------------------------------ dequantise into TMEM
-    // warp pair (w, w + 4) shares lane quarter q; half h dequantises block h
-    // of each 64-input k-step (TMEM columns 16h .. 16h+15 of the stage).
+    // warp pair (w, w + 4) shares lane quarter q; half h dequantises blocks
+    // 2h and 2h + 1 of each 128-input k-step (TMEM columns 32h .. 32h+31 of
+    // the stage).
     const int q = warp & 3;
     const int h = (warp - PF_DQ0) >> 2;
     const int m = 32 * q + lane;                          // A row = TMEM lane
@@ -805,45 +820,59 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
         const uint8_t* st = sraw + r * PF_RAW_STAGE;
         const int nk = min(RKS, KS - g * RKS);
         const uint4 scv = *reinterpret_cast<const uint4*>(st + soff);
-        // block 2j + h of the stage: IQ4_NL 16 bytes (chunk 2j + h), Q8_0 32 bytes (chunks 2(2j + h), +1)
+        // block b = 2h + i of the stage's k-step j: IQ4_NL 16 bytes (chunk 4j + b),
+        // Q8_0 32 bytes (chunks 2b, 2b + 1; one k-step a stage)
         constexpr int NCH = WF == MOEX_Q8_0 ? 2 : 1;
-        uint4 qv[RKS][NCH];
+        uint4 qv[RKS][2][NCH];
 #pragma unroll
         for (int j = 0; j < RKS; ++j)
 #pragma unroll
-          for (int c = 0; c < NCH; ++c)
-            if (j < nk) qv[j][c] = *reinterpret_cast<const uint4*>(st + qoff + (((NCH * (2 * j + h) + c) ^ (rr & 7)) << 4));
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int c = 0; c < NCH; ++c)
+              if (j < nk) {
+                const int chunk = WF == MOEX_Q8_0 ? 2 * (2 * h + i) + c : 4 * j + 2 * h + i;
+                qv[j][i][c] = *reinterpret_cast<const uint4*>(st + qoff + ((chunk ^ (rr & 7)) << 4));
+              }
         __syncwarp();
         if (lane == 0) mbar_arrive(&r_empty[r]);  // the raw bytes are in registers
         const uint32_t sw[4] = {scv.x, scv.y, scv.z, scv.w};
 #pragma unroll
         for (int j = 0; j < RKS; ++j) {
           if (j >= nk) break;
-          // scale of block 2k + h of the 4 k-steps the 16 scale bytes cover: 16-bit half h of word k
-          uint32_t swv = sw[j];
-          if (WF == MOEX_Q8_0 && (g & 1)) swv = sw[j + 2 < 4 ? j + 2 : 3];
-          const uint16_t dbits = static_cast<uint16_t>(h ? (swv >> 16) : (swv & 0xFFFFu));
-          uint32_t col[16];
-          if constexpr (WF == MOEX_Q8_0)
-            dequant_q8_block16(qv[j][0], qv[j][NCH - 1], dbits, col);
-          else
-            dequant_block16(qv[j][0], dbits, col);
-          const int s = kc % PF_NA_ST;
-          if (kc >= PF_NA_ST && !mbar_wait(&ab_empty[s], ((kc / PF_NA_ST) - 1) & 1, abort_flag)) {
+          const int ks = g * RKS + j;
+          // a half last k-step has blocks 0 and 1 only
+          const bool has = !(half_last && ks == KS - 1 && h == 1);
+          const int sa = kc % PF_NA_ST;
+          const int j0 = kc - PF_NA_ST;  // the k-step that used this A stage before
+          if (j0 >= 0 && !mbar_wait(&kdone[j0 % PF_KD], (j0 / PF_KD) & 1, abort_flag)) {
             *abort_flag = 1;
             flag_status(a.status, DEV_TIMEOUT_MMA);
             break;
           }
           tc_fence_after();
-          tmem_st16(tmem + (static_cast<uint32_t>(32 * q) << 16) + PF_ACOL + s * 32 + 16 * h, col);
-          tmem_st_wait();
+          if (has) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              // scale of block b = 2h + i: word 2j + h (Q8_0: 2 (g & 1) + h) of the 8 scales, half i
+              const uint32_t swv = sw[WF == MOEX_Q8_0 ? 2 * (g & 1) + h : 2 * j + h];
+              const uint16_t dbits = static_cast<uint16_t>(i ? (swv >> 16) : (swv & 0xFFFFu));
+              uint32_t col[16];
+              if constexpr (WF == MOEX_Q8_0)
+                dequant_q8_block16(qv[j][i][0], qv[j][i][NCH - 1], dbits, col);
+              else
+                dequant_block16(qv[j][i][0], dbits, col);
+              tmem_st16(tmem + (static_cast<uint32_t>(32 * q) << 16) + PF_ACOL + sa * PF_ACOLS + 32 * h + 16 * i, col);
+            }
+            tmem_st_wait();
+          }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) {  // the warp's 32 rows of this block are in TMEM
+          if (lane == 0) {  // the warp's 32 rows of these blocks are in TMEM
             if (PAIR && rank == 1)
-              mbar_arrive_remote(full_mma + 8u * s);
+              mbar_arrive_remote(full_mma + 8u * sa);
             else
-              mbar_arrive(&full[s]);
+              mbar_arrive(&full[sa]);
           }
           ++kc;
         }
@@ -1219,7 +1248,7 @@ bool make_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int boxr) 
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
-  const cuuint32_t box[2] = {PF_BK, static_cast<cuuint32_t>(boxr)};
+  const cuuint32_t box[2] = {PF_BOXK, static_cast<cuuint32_t>(boxr)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
