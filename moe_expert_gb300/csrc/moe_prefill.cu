@@ -468,10 +468,10 @@ struct PfSmem {
 template <bool PAIR>
 __host__ __device__ constexpr int pf_boxr() { return PAIR ? 96 : 192; }
 
-// MMA N of a sub-tile of `nrows` tokens: a multiple of 16 (one CTA) or of 32
-// (a pair, whose CTAs hold N/2 rows each).
+// MMA N of a sub-tile of `nrows` tokens: a multiple of 16 (for a pair each
+// CTA holds N/2 rows, a multiple of 8: whole 8-row swizzle atoms).
 template <bool PAIR>
-__device__ __forceinline__ int pf_mma_n(int nrows) { return PAIR ? (nrows + 31) & ~31 : (nrows + 15) & ~15; }
+__device__ __forceinline__ int pf_mma_n(int nrows) { return (nrows + 15) & ~15; }
 
 // How a tile of `rows` tokens is laid out: sub-tile h (h = 0, 1) covers tile
 // rows [start[h], start[h] + rows[h]) with MMA width n[h] into TMEM slot h
