@@ -46,12 +46,18 @@ constexpr int PF_CAP_PAIR = 384; // tokens of a tile for CTA pairs: two sub-tile
 constexpr int PF_CAP_ONE = 192;  // tokens of a tile for single CTAs: one sub-tile
 constexpr int PF_BK = 128;       // inputs per k-step (two 128-byte swizzle rows of FP16); K's last may be 64
 constexpr int PF_BOXK = 64;      // inputs per token-row TMA box (one 128-byte swizzle row)
-constexpr int PF_NB_ST = 3;      // B (token) stages in shared memory
+constexpr int PF_B_BYTES = 3 * 2 * 192 * 64 * 2;  // shared memory of the B (token) stages: 144 KB
+constexpr int PF_NB_MAX = 6;     // most B stages (CTAs of a MoE pair: 96 rows, 24 KB a stage)
 constexpr int PF_NA_ST = 2;      // A (weight) stages in TMEM
 constexpr int PF_KD = 6;         // k-step-done barriers: k-step kc's MMAs commit to kdone[kc % 6]
-static_assert(PF_KD % PF_NB_ST == 0 && PF_KD % PF_NA_ST == 0, "a k-step's stages free on its own barrier");
-constexpr int PF_HALF_B = 192 * PF_BOXK * 2;      // bytes of one 64-input half of a B stage: at most 192 token rows a CTA
-constexpr int PF_STAGE_B = 2 * PF_HALF_B;         // bytes of one B stage
+static_assert(PF_KD % PF_NA_ST == 0, "a k-step's stages free on its own barrier");
+
+// Token rows a CTA holds of a tile: 96 for a CTA of a MoE pair (tiles of at
+// most 192 rows, one sub-tile), 192 otherwise (one CTA; or the dense pair's
+// two sub-tiles of up to 96 rows each).  The B stages take PF_B_BYTES: six
+// stages of 24 KB or three of 48 KB.
+template <int EPI, bool PAIR>
+__host__ __device__ constexpr int pf_rows_cta() { return PAIR && EPI != 3 ? 96 : 192; }
 constexpr int PF_ACOL = 2 * PF_SUBN;              // first TMEM column of the A stages (after two slots)
 constexpr int PF_ACOLS = PF_BK / 2;               // TMEM columns of one A stage (FP16 pairs)
 static_assert(PF_ACOL + PF_NA_ST * PF_ACOLS <= 512, "accumulators and A stages fit the TMEM");
@@ -448,9 +454,9 @@ struct PfSmem {
   int b, raw, bars, xch, tmem, abort_flag, total;
   __host__ __device__ PfSmem() {
     int o = 0;
-    b = o; o += PF_NB_ST * PF_STAGE_B;                          // 1024-aligned (dynamic smem base)
+    b = o; o += PF_B_BYTES;                                     // 1024-aligned (dynamic smem base)
     raw = o; o += PF_NR_ST * PF_RAW_STAGE;                      // 1024-aligned
-    bars = o; o += 8 * (2 * PF_NB_ST + PF_KD + PF_NA_ST + 2 * PF_NR_ST + 4 + 1);
+    bars = o; o += 8 * (2 * PF_NB_MAX + PF_KD + PF_NA_ST + 2 * PF_NR_ST + 4 + 1);
     o = (o + 15) & ~15;
     xch = o; o += 4 * 2 * 2 * 32 * 4;                          // integer route: per warp pair, amax and sums of 32 columns
     tmem = o; o += 16;
@@ -537,15 +543,19 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const PfSmem L;
+  constexpr int HALF_B = pf_rows_cta<EPI, PAIR>() * PF_BOXK * 2;  // bytes of one 64-input half of a B stage
+  constexpr int STAGE_B = 2 * HALF_B;                              // bytes of one B stage
+  constexpr int NB = PF_B_BYTES / STAGE_B;                         // B stages
+  static_assert(NB <= PF_NB_MAX && PF_KD % NB == 0, "B stages free on the k-step-done ring");
   uint8_t* sb = smem + L.b;
   uint8_t* sraw = smem + L.raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-  // k-step kc uses B stage kc % PF_NB_ST and A stage kc % PF_NA_ST; its one
+  // k-step kc uses B stage kc % NB and A stage kc % PF_NA_ST; its one
   // MMA commit (for a pair, to both CTAs) completes kdone[kc % PF_KD], which
   // frees both stages
   uint64_t* b_full = bars;                  // this CTA's B stage has landed
-  uint64_t* b_peer = b_full + PF_NB_ST;     // (issuing CTA of a pair) the odd CTA's B stage has landed
-  uint64_t* kdone = b_peer + PF_NB_ST;
+  uint64_t* b_peer = b_full + NB;     // (issuing CTA of a pair) the odd CTA's B stage has landed
+  uint64_t* kdone = b_peer + NB;
   // full[s] (on the CTA that issues the MMAs): the A stage is in TMEM in
   // every CTA of the pair (each dequantising warp arrives; the odd CTA's
   // remotely)
@@ -563,7 +573,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < PF_NB_ST; ++i) {
+    for (int i = 0; i < NB; ++i) {
       mbar_init(&b_full[i], 1);
       mbar_init(&b_peer[i], 1);     // the odd CTA's forwarder
     }
@@ -624,8 +634,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
         for (int h = 0; h < 2; ++h) src[h] = tile.z + st.start[h] + (PAIR ? rank * (st.n[h] / 2) : 0);
         const uint32_t half_bytes = (st.nbox[0] + st.nbox[1]) * BOXR * PF_BOXK * 2;
         for (int ks = 0; ks < KS; ++ks, ++kc) {
-          const int s = kc % PF_NB_ST;
-          const int j0 = kc - PF_NB_ST;  // the k-step that used this stage before
+          const int s = kc % NB;
+          const int j0 = kc - NB;  // the k-step that used this stage before
           if (j0 >= 0 && !mbar_wait(&kdone[j0 % PF_KD], (j0 / PF_KD) & 1, abort_flag)) {
             *abort_flag = 1;
             flag_status(a.status, DEV_TIMEOUT_MMA);
@@ -637,14 +647,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
 #pragma unroll
             for (int h = 0; h < 2; ++h)
               for (int bx = 0; bx < st.nbox[h]; ++bx)
-                tma_load_2d(sb + s * PF_STAGE_B + j * PF_HALF_B + (st.off[h] + bx * BOXR) * PF_BOXK * 2, &bmap,
+                tma_load_2d(sb + s * STAGE_B + j * HALF_B + (st.off[h] + bx * BOXR) * PF_BOXK * 2, &bmap,
                             ks * PF_BK + j * PF_BOXK, src[h] + BOXR * bx, &b_full[s]);
         }
       }
       // after an abort, let the copies already issued land before the CTA exits
       if (*abort_flag) {
-        for (int j = kc - 1; j >= 0 && j >= kc - PF_NB_ST; --j)
-          mbar_wait(&b_full[j % PF_NB_ST], (j / PF_NB_ST) & 1, nullptr);
+        for (int j = kc - 1; j >= 0 && j >= kc - NB; --j)
+          mbar_wait(&b_full[j % NB], (j / NB) & 1, nullptr);
       }
     }
   } else if (warp == 1 && PAIR && rank == 1) {
@@ -657,8 +667,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
       int kc = 0;
       for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
         for (int ks = 0; ks < KS; ++ks, ++kc) {
-          const int s = kc % PF_NB_ST;
-          if (!mbar_wait(&b_full[s], (kc / PF_NB_ST) & 1, abort_flag)) {
+          const int s = kc % NB;
+          if (!mbar_wait(&b_full[s], (kc / NB) & 1, abort_flag)) {
             *abort_flag = 1;
             flag_status(a.status, DEV_TIMEOUT_MMA);
             break;
@@ -707,9 +717,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
           break;
         }
         for (int ks = 0; ks < KS; ++ks, ++kc) {
-          const int sb_ = kc % PF_NB_ST, sa = kc % PF_NA_ST;
-          if (!mbar_wait(&b_full[sb_], (kc / PF_NB_ST) & 1, abort_flag) ||
-              (PAIR && !mbar_wait(&b_peer[sb_], (kc / PF_NB_ST) & 1, abort_flag)) ||
+          const int sb_ = kc % NB, sa = kc % PF_NA_ST;
+          if (!mbar_wait(&b_full[sb_], (kc / NB) & 1, abort_flag) ||
+              (PAIR && !mbar_wait(&b_peer[sb_], (kc / NB) & 1, abort_flag)) ||
               !mbar_wait(&full[sa], (kc / PF_NA_ST) & 1, abort_flag)) {
             *abort_flag = 1;
             flag_status(a.status, DEV_TIMEOUT_MMA);
@@ -717,12 +727,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
           }
           tc_fence_after();
           const uint32_t acol = tmem + PF_ACOL + sa * PF_ACOLS;
-          const uint64_t boff = static_cast<uint64_t>((sb_ * PF_STAGE_B) >> 4);
+          const uint64_t boff = static_cast<uint64_t>((sb_ * STAGE_B) >> 4);
           const int nkk = (half_last && ks == KS - 1) ? PF_BOXK / 16 : PF_BK / 16;
           for (int h = 0; h < nh; ++h) {
             for (int kk = 0; kk < nkk; ++kk) {
               // 16-input step kk: half kk / 4 of the stage, 32 bytes further per step within it
-              const uint64_t bd = bdesc[h] + boff + (kk >> 2) * (PF_HALF_B >> 4) + 2 * (kk & 3);
+              const uint64_t bd = bdesc[h] + boff + (kk >> 2) * (HALF_B >> 4) + 2 * (kk & 3);
               if constexpr (PAIR)
                 mma_f16_ts_pair(dcol[h], acol + kk * 8, bd, idesc[h], (ks | kk) != 0);
               else
