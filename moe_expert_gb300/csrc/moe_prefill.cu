@@ -105,10 +105,10 @@ __host__ __device__ inline void pf_tile_span(int n, int cap, int t, int* r0, int
 
 constexpr int PF_MAX_SEGS = 1024;   // at most this many histogram segments
 
-// Entries per segment: a multiple of 32, at least 512, at most PF_MAX_SEGS segments.
+// Entries per segment: a multiple of 32, at least 256, at most PF_MAX_SEGS segments.
 __host__ __device__ inline int pf_seg_len(int n) {
   int seg = (n + PF_MAX_SEGS - 1) / PF_MAX_SEGS;
-  seg = seg < 512 ? 512 : seg;
+  seg = seg < 256 ? 256 : seg;
   return (seg + 31) & ~31;
 }
 __host__ __device__ inline int pf_nsegs(int n) { return (n + pf_seg_len(n) - 1) / pf_seg_len(n); }
@@ -170,9 +170,60 @@ __global__ void __launch_bounds__(1024) prefill_scan_kernel(int n, int E, int* _
                                                             int* __restrict__ counts, int* __restrict__ eoff,
                                                             int* __restrict__ etb, PrefillTiles tl) {
   __shared__ int red[32];
+  __shared__ int part[1024];    // [segment group][expert]: partial counts, then their exclusive prefix
+  __shared__ int eoff_s[512];
   pdl_wait();
   pdl_launch_dependents();
   const int S = pf_nsegs(n);
+  if (E <= 512) {
+    // G groups of segments per expert, one thread each (a warp reads 32
+    // experts of one segment: coalesced)
+    const int G = 1024 / E;
+    const int t = threadIdx.x, e = t % E, gr = t / E;
+    const int s0 = gr < G ? S * gr / G : 0, s1 = gr < G ? S * (gr + 1) / G : 0;
+    int v = 0;
+    for (int sg = s0; sg < s1; ++sg) v += hist[static_cast<int64_t>(sg) * E + e];
+    if (gr < G) part[gr * E + e] = v;
+    __syncthreads();
+    int c = 0, tiles = 0;
+    if (t < E) {
+      for (int g = 0; g < G; ++g) {  // the groups' exclusive prefix, in segment order
+        const int x = part[g * E + t];
+        part[g * E + t] = c;
+        c += x;
+      }
+      tiles = pf_token_tiles(c, tl.cap);
+    }
+    int off = c, tb = tiles;
+    const int placed = block_exscan(off, red);
+    const int ttot = block_exscan(tb, red);
+    if (t == 0) {
+      tl.n1[0] = ttot * tl.F1;
+      tl.n1[1] = ttot * tl.F2;
+      tl.n1[2] = placed;
+      tl.n1[3] = ttot;
+      etb[E] = ttot;
+    }
+    if (t < E) {
+      counts[t] = c;
+      eoff[t] = off;
+      etb[t] = tb;
+      eoff_s[t] = off;
+    }
+    __syncthreads();
+    // hist[s][e] becomes the first sorted row of segment s's entries of e
+    if (gr < G) {
+      int run = eoff_s[e] + part[gr * E + e];
+      for (int sg = s0; sg < s1; ++sg) {
+        int* hp = hist + static_cast<int64_t>(sg) * E + e;
+        const int h = *hp;
+        *hp = run;
+        run += h;
+      }
+    }
+    return;
+  }
+  // more experts: four a thread, segments in series
   int c[4];
   int csum = 0, tsum = 0;
 #pragma unroll
