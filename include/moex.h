@@ -215,8 +215,9 @@ size_t moex_moe_prefill_workspace_bytes(int T, int k, int E, int64_t hidden, int
 
 /*
  * Byte offsets of the prefill workspace's parts, for inspection by tests:
- * offsets[0] counts int32[E] (then the sort's per-segment histograms and
- * per-expert offsets), [1] order int32[T*k] (entry index of each sorted row),
+ * offsets[0] counts int32[E] (then the sort's per-segment histograms,
+ * per-expert offsets and each entry's sorted row, -1 for an entry left out),
+ * [1] order int32[T*k] (entry index of each sorted row),
  * [2] {token, weight bits} int32x2[T*k], [3]/[4] tile lists, [5] totals
  * int32[4] (GEMM 1 tiles, GEMM 2 tiles, placed rows, token tiles), [6] Xs
  * FP16 [T*k][hidden] (gathered rows), [7] Hs FP16
@@ -256,7 +257,8 @@ size_t moex_moe_prefill_q8_workspace_bytes(int T, int k, int E, int64_t hidden, 
 
 /*
  * Byte offsets of the integer-route workspace: offsets[0] counts (then the
- * sort's histograms and expert offsets), [1] order int32[T*k], [2] {token,
+ * sort's histograms, expert offsets and each entry's sorted row), [1] order
+ * int32[T*k], [2] {token,
  * weight bits} int32x2[T*k], [3] first-product tile list, [4] down-product
  * tile list, [5] totals, [6] Xs FP16 [T*k][hidden] (interleaved blocks as in
  * the FP16 route), [7] Hq int8 [T*k][inter] (natural order), [8] {d, s}

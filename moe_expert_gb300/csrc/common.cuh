@@ -204,6 +204,17 @@ constexpr uint32_t IQ4NL_LO7_1 = 0x766A5D4Fu;   // -49,-35,-22,-10 & 0x7f
 constexpr uint32_t IQ4NL_HI_0 = 0x26190D01u;    // 1,13,25,38
 constexpr uint32_t IQ4NL_HI_1 = 0x71594535u;    // 53,69,89,113
 
+// The same codebook as two tables for a split dot product: low entries as
+// they are (all negative, so prmt's sign-replicate gives -1 where the index
+// is >= 8), high entries plus one (all positive, so the flipped selector gives
+// 0 where the index is < 8).  The byte-wise sum of the two lookups is the
+// codebook value everywhere, so two dp4a's with the same activations give the
+// exact integer dot.
+constexpr uint32_t IQ4NL_LO_0 = 0xBFAD9881u;    // -127,-104,-83,-65
+constexpr uint32_t IQ4NL_LO_1 = 0xF6EADDCFu;    // -49,-35,-22,-10
+constexpr uint32_t IQ4NL_HIP1_0 = 0x271A0E02u;  // 2,14,26,39
+constexpr uint32_t IQ4NL_HIP1_1 = 0x725A4636u;  // 54,70,90,114
+
 // Decodes the four 4-bit codebook indices held in the low 16 bits of `sel`
 // (nibble k -> output byte k) into four int8 codebook values.
 //   lo7: entries 0..7 with bit 7 cleared, 0 where the index is >= 8 (prmt's

@@ -114,6 +114,33 @@ __device__ __forceinline__ void load_act(ActRegs<FMT, C>& r, const int8_t* const
 template <int FMT, int C>
 __device__ __forceinline__ void block_dots_from(uint4 q0, uint4 q1, float dw, const ActRegs<FMT, C>& act, float* p,
                                                 int* I_out = nullptr) {
+  if constexpr (FMT != MOEX_Q8_0 && C <= 2) {
+    // one or two columns: two table lookups and two dp4a's per four weights
+    // (split codebook) cost fewer instructions than rebuilding the values
+    (void)q1;
+    const uint32_t W[4] = {q0.x, q0.y, q0.z, q0.w};
+    int I[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) I[c] = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t fl = W[i] ^ 0x88888888u;
+      const uint32_t sel[2] = {W[i], W[i] >> 16}, self[2] = {fl, fl >> 16};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t lo = prmt(IQ4NL_LO_0, IQ4NL_LO_1, sel[h]);
+        const uint32_t hi = prmt(IQ4NL_HIP1_0, IQ4NL_HIP1_1, self[h]);
+#pragma unroll
+        for (int c = 0; c < C; ++c) I[c] = dp4a(hi, act.a[c][2 * i + h], dp4a(lo, act.a[c][2 * i + h], I[c]));
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      if (I_out) I_out[c] = I[c];
+      p[c] = __fmul_rn(__int2float_rn(I[c]), __fmul_rn(dw, act.d[c]));
+    }
+    return;
+  }
   uint32_t wv[8];
   if constexpr (FMT == MOEX_Q8_0) {
     wv[0] = q0.x; wv[1] = q0.y; wv[2] = q0.z; wv[3] = q0.w;

@@ -313,12 +313,13 @@ __global__ void __launch_bounds__(256) dense_tiles_kernel(int T, int F, int cap,
 }
 
 // One warp per segment, entries in order, 32 at a time: equal experts are
-// ranked by lane with __match_any_sync; order[row] = entry, tokw[row] =
+// ranked by lane with __match_any_sync; order[row] = entry, pos[entry] = row
+// (-1 for an entry left out), tokw[row] =
 // {token, weight bits}.
 __global__ void __launch_bounds__(32) prefill_scatter_kernel(const int32_t* __restrict__ ids,
                                                              const float* __restrict__ w, int n, int k, int E,
                                                              const int* __restrict__ hist, int* __restrict__ order,
-                                                             int2* __restrict__ tokw) {
+                                                             int2* __restrict__ tokw, int* __restrict__ pos) {
   extern __shared__ int run[];
   pdl_wait();
   pdl_launch_dependents();
@@ -332,12 +333,13 @@ __global__ void __launch_bounds__(32) prefill_scatter_kernel(const int32_t* __re
     const int v = j < j1 ? ids[j] : -1;
     const bool ok = v >= 0 && v < E;
     const unsigned peers = __match_any_sync(0xffffffffu, ok ? v : -1);
+    int row = -1;
     if (ok) {
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      const int row = run[v] + rank;
+      row = run[v] + __popc(peers & ((1u << lane) - 1u));
       order[row] = j;
       tokw[row] = make_int2(j / k, __float_as_int(w[j]));
     }
+    if (j < j1) pos[j] = row;
     __syncwarp();
     // the highest lane of each group advances the expert's next row
     if (ok && (peers >> lane) == 1u) run[v] += __popc(peers);
@@ -347,47 +349,66 @@ __global__ void __launch_bounds__(32) prefill_scatter_kernel(const int32_t* __re
 
 // ----------------------------------------------------------------- gather
 
-// Xs[p] = fp16(x[token(order[p])]) with each 32-input block interleaved,
-// for the placed rows p < *nrows.  One thread per 32-input block: 64 bytes
-// in, 64 bytes out, all four 16-byte loads issued before any convert.  The
-// same threads initialise the layer output (out_vec4 float4s), which the
-// second GEMM accumulates into: zeros, or the residual when one is given
-// (which may be out itself), so no separate pass sits between the GEMMs.
-__global__ void __launch_bounds__(256) prefill_gather_kernel(const uint16_t* __restrict__ x, int H, int k,
-                                                             const int* __restrict__ nrows,
-                                                             const int* __restrict__ order, __half* __restrict__ xs,
+// Xs[pos[t*k+s]] = fp16(x[t]) for every entry (t, s) placed by the sort
+// (pos[] < 0: left out; pos == nullptr: the dense product, row t), with each
+// 32-input block interleaved (FP16 word j of a block holds inputs j and
+// j + 16).  One warp per token, in token order, so each input row is read
+// from memory once and written to its k sorted rows.  Lane l takes 16-byte
+// quarters q of the row's blocks (quarter index 4 * block + q = l, l + 32,
+// ...), so a warp's stores cover 512 contiguous bytes; a quarter's inputs
+// are the two 8-byte runs 4q..4q+3 and 16+4q..19+4q of the block.  The same
+// threads initialise the layer output (out_vec4 float4s), which the second
+// GEMM accumulates into: zeros, or the residual when one is given (which may
+// be out itself), so no separate pass sits between the GEMMs.
+__global__ void __launch_bounds__(256) prefill_gather_kernel(const uint16_t* __restrict__ x, int H, int T, int k,
+                                                             const int* __restrict__ pos, __half* __restrict__ xs,
                                                              const float4* res, float4* out, int64_t out_vec4) {
+  constexpr int CH = 4;  // quarters a lane converts before its k rows of stores
   pdl_wait();
   pdl_launch_dependents();
-  const int per_row = H / QK;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t z = i; z < out_vec4; z += nthreads) out[z] = res ? res[z] : make_float4(0.f, 0.f, 0.f, 0.f);
-  const int64_t row = i / per_row;
-  if (row >= *nrows) return;
-  const int blk = static_cast<int>(i - row * per_row);
-  const int t = order ? order[row] / k : static_cast<int>(row);  // dense: rows are tokens
-  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H + blk * QK);
-  uint32_t in[16];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint4 v = __ldg(src + j);
-    in[4 * j] = v.x; in[4 * j + 1] = v.y; in[4 * j + 2] = v.z; in[4 * j + 3] = v.w;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int lane = threadIdx.x & 31;
+  int myrow = -1;  // lane s < k: the sorted row of entry (t, s)
+  if (pos) {
+    if (lane < k) myrow = pos[static_cast<int64_t>(t) * k + lane];
+  } else if (lane == 0) {
+    myrow = t;
   }
-  // element e of the block: 16-bit half (e & 1) of word e >> 1
-  auto elem = [&](int e) -> float {
-    const uint32_t wv = in[e >> 1];
-    return __uint_as_float((e & 1) ? (wv & 0xFFFF0000u) : (wv << 16));
-  };
-  uint32_t o[16];
+  const int nq = 4 * (H / QK);
+  const uint2* src = reinterpret_cast<const uint2*>(x + static_cast<int64_t>(t) * H);
+  for (int q0 = 0; q0 < nq; q0 += 32 * CH) {
+    uint4 o[CH];
 #pragma unroll
-  for (int jj = 0; jj < 16; ++jj) {
-    const __half2 h = __halves2half2(__float2half_rn(elem(jj)), __float2half_rn(elem(jj + 16)));
-    o[jj] = *reinterpret_cast<const uint32_t*>(&h);
+    for (int c = 0; c < CH; ++c) {
+      const int qi = q0 + 32 * c + lane;
+      if (qi >= nq) break;
+      const int q = qi & 3;
+      const uint2 lo = __ldg(src + 2 * (qi - q) + q), hi = __ldg(src + 2 * (qi - q) + 4 + q);
+      // a BF16 is the upper half of an FP32; each FP16 pair (4q + j, 16 + 4q + j)
+      // is one round-to-nearest conversion of two FP32s, the first in the low half
+      const uint32_t a[4] = {lo.x << 16, lo.x & 0xFFFF0000u, lo.y << 16, lo.y & 0xFFFF0000u};
+      const uint32_t b[4] = {hi.x << 16, hi.x & 0xFFFF0000u, hi.y << 16, hi.y & 0xFFFF0000u};
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w[j]) : "f"(__uint_as_float(b[j])), "f"(__uint_as_float(a[j])));
+      o[c] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    for (int sl = 0; sl < k; ++sl) {
+      const int row = __shfl_sync(0xffffffffu, myrow, sl);
+      if (row < 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(xs + static_cast<int64_t>(row) * H);
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int qi = q0 + 32 * c + lane;
+        if (qi < nq) dst[qi] = o[c];
+      }
+    }
   }
-  uint4* dst = reinterpret_cast<uint4*>(xs + row * H + blk * QK);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
 }
 
 // ----------------------------------------------------------------- GEMM
@@ -1413,7 +1434,7 @@ void prefill_ws_layout(int T, int k, int E, int64_t hidden, int64_t inter, size_
   const size_t tiles = n / PF_CAP_ONE + E + 1;   // token tiles of both tile caps fit
   const size_t segs = static_cast<size_t>(pf_nsegs(static_cast<int>(n)));
   size_t o = 0;
-  off[0] = o; o = align_up(o + 4 * E + 4 * segs * E + 8 * E + 4, 256);  // counts, segment histograms, eoff, etb
+  off[0] = o; o = align_up(o + 4 * E + 4 * segs * E + 8 * E + 4 + 4 * n, 256);  // counts, segment histograms, eoff, etb, pos
   off[1] = o; o = align_up(o + 4 * n, 256);                              // order
   off[2] = o; o = align_up(o + 8 * n, 256);                              // tokw
   off[3] = o; o = align_up(o + 16 * tiles * (inter / 64), 256);          // tiles 1
@@ -1478,13 +1499,12 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
                  static_cast<const int*>(counts), static_cast<const int*>(eoff), static_cast<const int*>(etb),
                  tl) != cudaSuccess)
     return MOEX_ECUDA;
+  int* pos = etb + E + 1;  // each entry's sorted row
   if (launch_pdl(prefill_scatter_kernel, dim3(S), dim3(32), esm, s, ids, w, n, k, E, static_cast<const int*>(hist),
-                 order, tokw) != cudaSuccess)
+                 order, tokw, pos) != cudaSuccess)
     return MOEX_ECUDA;
-  const int64_t gthreads = static_cast<int64_t>(n) * (H / QK);
-  if (launch_pdl(prefill_gather_kernel, dim3(static_cast<unsigned>((gthreads + 255) / 256)), dim3(256), 0, s, x, H,
-                 k, static_cast<const int*>(tl.n1 + 2), static_cast<const int*>(order), xs,
-                 reinterpret_cast<const float4*>(residual), reinterpret_cast<float4*>(out),
+  if (launch_pdl(prefill_gather_kernel, dim3(static_cast<unsigned>((T + 7) / 8)), dim3(256), 0, s, x, H, T, k,
+                 static_cast<const int*>(pos), xs, reinterpret_cast<const float4*>(residual), reinterpret_cast<float4*>(out),
                  static_cast<int64_t>(T) * H / 4) != cudaSuccess)
     return MOEX_ECUDA;
   const PfSmem L;
@@ -1530,7 +1550,7 @@ void prefill_q8_ws_layout(int T, int k, int E, int64_t hidden, int64_t inter, si
   const size_t n = static_cast<size_t>(T) * k;
   const size_t segs = static_cast<size_t>(pf_nsegs(static_cast<int>(n)));
   size_t o = 0;
-  off[0] = o; o = align_up(o + 4 * E + 4 * segs * E + 8 * E + 4, 256);
+  off[0] = o; o = align_up(o + 4 * E + 4 * segs * E + 8 * E + 4 + 4 * n, 256);
   off[1] = o; o = align_up(o + 4 * n, 256);
   off[2] = o; o = align_up(o + 8 * n, 256);
   off[3] = o; o = align_up(o + 16 * (n / PF_CAP_ONE + E + 1) * (inter / 64), 256);
@@ -1595,13 +1615,12 @@ moex_status launch_moe_prefill_q8(const moex_qweight* gu, const moex_qweight* dn
   if (launch_pdl(q8_tiles_kernel, dim3(1), dim3(1024), 0, s, E, H / QD_ROWS, static_cast<const int*>(counts),
                  static_cast<const int*>(eoff), qt, nq) != cudaSuccess)
     return MOEX_ECUDA;
+  int* pos = etb + E + 1;  // each entry's sorted row
   if (launch_pdl(prefill_scatter_kernel, dim3(S), dim3(32), esm, s, ids, w, n, k, E, static_cast<const int*>(hist),
-                 order, tokw) != cudaSuccess)
+                 order, tokw, pos) != cudaSuccess)
     return MOEX_ECUDA;
-  const int64_t gthreads = static_cast<int64_t>(n) * (H / QK);
-  if (launch_pdl(prefill_gather_kernel, dim3(static_cast<unsigned>((gthreads + 255) / 256)), dim3(256), 0, s, x, H,
-                 k, static_cast<const int*>(tl.n1 + 2), static_cast<const int*>(order), xs,
-                 static_cast<const float4*>(nullptr), reinterpret_cast<float4*>(out),
+  if (launch_pdl(prefill_gather_kernel, dim3(static_cast<unsigned>((T + 7) / 8)), dim3(256), 0, s, x, H, T, k,
+                 static_cast<const int*>(pos), xs, static_cast<const float4*>(nullptr), reinterpret_cast<float4*>(out),
                  static_cast<int64_t>(T) * H / 4) != cudaSuccess)
     return MOEX_ECUDA;
   const PfSmem L;
@@ -1679,10 +1698,9 @@ moex_status launch_dense_prefill(const moex_qweight* W, const uint16_t* x, int T
   const int ntiles = pf_token_tiles(T, cap) * F;
   if (launch_pdl(dense_tiles_kernel, dim3((ntiles + 255) / 256), dim3(256), 0, s, T, F, cap, tiles, n1) != cudaSuccess)
     return MOEX_ECUDA;
-  const int64_t gthreads = static_cast<int64_t>(T) * (K / QK);
-  if (launch_pdl(prefill_gather_kernel, dim3(static_cast<unsigned>((gthreads + 255) / 256)), dim3(256), 0, s, x, K, 1,
-                 static_cast<const int*>(n1 + 2), static_cast<const int*>(nullptr), xs,
-                 static_cast<const float4*>(nullptr), static_cast<float4*>(nullptr), int64_t(0)) != cudaSuccess)
+  if (launch_pdl(prefill_gather_kernel, dim3(static_cast<unsigned>((T + 7) / 8)), dim3(256), 0, s, x, K, T, 1,
+                 static_cast<const int*>(nullptr), xs, static_cast<const float4*>(nullptr), static_cast<float4*>(nullptr),
+                 int64_t(0)) != cudaSuccess)
     return MOEX_ECUDA;
   const PfSmem L;
   const PfKernel kern = pf_kernel<3>(cl, W->fmt);
