@@ -267,12 +267,16 @@ __global__ void __launch_bounds__(1024) prefill_scan_kernel(int n, int E, int* _
 
 // Both tile lists, one thread per tile: token tile g belongs to the last
 // expert e with etb[e] <= g; its ceil(n_e / cap) token tiles split the
-// expert's rows evenly.
+// expert's rows evenly.  etb[0..E] is staged in shared memory (E + 1 ints)
+// for the binary search.
 __global__ void __launch_bounds__(256) prefill_tiles_kernel(int E, const int* __restrict__ counts,
                                                             const int* __restrict__ eoff, const int* __restrict__ etb,
                                                             PrefillTiles tl) {
+  extern __shared__ int etb_s[];
   pdl_wait();
   pdl_launch_dependents();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) etb_s[e] = etb[e];
+  __syncthreads();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t TT = tl.n1[3];
   const bool first = i < TT * tl.F1;
@@ -283,7 +287,7 @@ __global__ void __launch_bounds__(256) prefill_tiles_kernel(int E, const int* __
   int lo = 0, hi = E;  // first e with etb[e] > g is in (lo, hi]
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (etb[mid] <= g) lo = mid; else hi = mid - 1;
+    if (etb_s[mid] <= g) lo = mid; else hi = mid - 1;
   }
   const int e = lo;
   int r0, rows;
@@ -328,22 +332,34 @@ __global__ void __launch_bounds__(32) prefill_scatter_kernel(const int32_t* __re
   __syncwarp();
   const int seg = pf_seg_len(n);
   const int j0 = blockIdx.x * seg, j1 = min(n, j0 + seg);
-  for (int jb = j0; jb < j1; jb += 32) {
-    const int j = jb + lane;
-    const int v = j < j1 ? ids[j] : -1;
-    const bool ok = v >= 0 && v < E;
-    const unsigned peers = __match_any_sync(0xffffffffu, ok ? v : -1);
-    int row = -1;
-    if (ok) {
-      row = run[v] + __popc(peers & ((1u << lane) - 1u));
-      order[row] = j;
-      tokw[row] = make_int2(j / k, __float_as_int(w[j]));
+  constexpr int SC = 8;  // 32-entry steps whose ids and weights are loaded up front
+  for (int jc = j0; jc < j1; jc += 32 * SC) {
+    int vv[SC];
+    float wv[SC];
+#pragma unroll
+    for (int u = 0; u < SC; ++u) {
+      const int j = jc + 32 * u + lane;
+      vv[u] = j < j1 ? ids[j] : -1;
+      wv[u] = j < j1 ? w[j] : 0.f;
     }
-    if (j < j1) pos[j] = row;
-    __syncwarp();
-    // the highest lane of each group advances the expert's next row
-    if (ok && (peers >> lane) == 1u) run[v] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < SC; ++u) {
+      const int j = jc + 32 * u + lane;
+      const int v = vv[u];
+      const bool ok = v >= 0 && v < E;
+      const unsigned peers = __match_any_sync(0xffffffffu, ok ? v : -1);
+      int row = -1;
+      if (ok) {
+        row = run[v] + __popc(peers & ((1u << lane) - 1u));
+        order[row] = j;
+        tokw[row] = make_int2(j / k, __float_as_int(wv[u]));
+      }
+      if (j < j1) pos[j] = row;
+      __syncwarp();
+      // the highest lane of each group advances the expert's next row
+      if (ok && (peers >> lane) == 1u) run[v] += __popc(peers);
+      __syncwarp();
+    }
   }
 }
 
@@ -356,10 +372,11 @@ __global__ void __launch_bounds__(32) prefill_scatter_kernel(const int32_t* __re
 // from memory once and written to its k sorted rows.  Lane l takes 16-byte
 // quarters q of the row's blocks (quarter index 4 * block + q = l, l + 32,
 // ...), so a warp's stores cover 512 contiguous bytes; a quarter's inputs
-// are the two 8-byte runs 4q..4q+3 and 16+4q..19+4q of the block.  The same
-// threads initialise the layer output (out_vec4 float4s), which the second
-// GEMM accumulates into: zeros, or the residual when one is given (which may
-// be out itself), so no separate pass sits between the GEMMs.
+// are the two 8-byte runs 4q..4q+3 and 16+4q..19+4q of the block.  Given
+// out_vec4 > 0 (the integer route), the same threads initialise the layer
+// output, which the down product accumulates into: zeros, or the residual
+// when one is given (which may be out itself).  In the FP16 route the first
+// GEMM's epilogue warps do that instead, under its MMAs.
 __global__ void __launch_bounds__(256) prefill_gather_kernel(const uint16_t* __restrict__ x, int H, int T, int k,
                                                              const int* __restrict__ pos, __half* __restrict__ xs,
                                                              const float4* res, float4* out, int64_t out_vec4) {
@@ -429,6 +446,12 @@ struct GemmArgs {
   float* out;          // GEMM 2 output [T][Hd]
   int Hd;
   const int2* tokw;    // per sorted row: token, weight bits
+  // GEMM 1 of the FP16 route: the layer output the second GEMM accumulates
+  // into, initialised to init_res (or zeros) as init_vec4 float4s, each CTA
+  // a contiguous slice, a piece after each of its tiles
+  float4* init_out;
+  const float4* init_res;
+  int64_t init_vec4;
   uint32_t* status;
 };
 
@@ -971,6 +994,22 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
     // the accumulator is released to the MMA thread's CTA (the even CTA of a pair)
     const uint32_t d_empty_mma = PAIR ? cluster_addr(smem_u32(d_empty), 0) : smem_u32(d_empty);
     int nsub = 0;  // as the MMA thread: sub-tile number i is in slot i & 1
+    // (GEMM 1) this CTA's slice of the output to initialise, spread over its
+    // tiles so that the writes stay a small share of the DRAM time, with
+    // streaming (evict-first) stores that leave the weights and token rows
+    // in L2
+    const int ethr = threadIdx.x - 32 * PF_EPI0;
+    int64_t zcur = a.init_vec4 * blockIdx.x / gridDim.x;
+    const int64_t zend = a.init_vec4 * (blockIdx.x + 1) / gridDim.x;
+    const int mytiles = t0 < ntiles ? (ntiles - t0 + tstep - 1) / tstep : 0;
+    const int64_t zchunk = (zend - zcur + mytiles - 1) / (mytiles > 0 ? mytiles : 1);
+    auto init_out_to = [&](int64_t zlim) {
+      if constexpr (EPI == 1) {
+        for (int64_t z = zcur + ethr; z < zlim; z += 32 * PF_EPI_WARPS)
+          __stcs(a.init_out + z, a.init_res ? __ldcs(a.init_res + z) : make_float4(0.f, 0.f, 0.f, 0.f));
+        zcur = zlim;
+      }
+    };
     int4 nxt = t0 < ntiles ? a.tiles[t0] : make_int4(0, 0, 0, 0);
     for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
       const int4 tile = nxt;
@@ -1104,7 +1143,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
             mbar_arrive(&d_empty[sl]);
         }
       }
+      init_out_to(zcur + zchunk < zend ? zcur + zchunk : zend);
     }
+    init_out_to(zend);  // a CTA without tiles (or one that stopped early)
   }
   tc_fence_before();
   __syncthreads();
@@ -1495,7 +1536,7 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   if (launch_pdl(prefill_scan_kernel, dim3(1), dim3(1024), 0, s, n, E, hist, counts, eoff, etb, tl) != cudaSuccess)
     return MOEX_ECUDA;
   const int64_t max_tiles = (static_cast<int64_t>(n) / PF_CAP_ONE + E + 1) * (tl.F1 + tl.F2);
-  if (launch_pdl(prefill_tiles_kernel, dim3(static_cast<unsigned>((max_tiles + 255) / 256)), dim3(256), 0, s, E,
+  if (launch_pdl(prefill_tiles_kernel, dim3(static_cast<unsigned>((max_tiles + 255) / 256)), dim3(256), esm + 4, s, E,
                  static_cast<const int*>(counts), static_cast<const int*>(eoff), static_cast<const int*>(etb),
                  tl) != cudaSuccess)
     return MOEX_ECUDA;
@@ -1504,8 +1545,8 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
                  order, tokw, pos) != cudaSuccess)
     return MOEX_ECUDA;
   if (launch_pdl(prefill_gather_kernel, dim3(static_cast<unsigned>((T + 7) / 8)), dim3(256), 0, s, x, H, T, k,
-                 static_cast<const int*>(pos), xs, reinterpret_cast<const float4*>(residual), reinterpret_cast<float4*>(out),
-                 static_cast<int64_t>(T) * H / 4) != cudaSuccess)
+                 static_cast<const int*>(pos), xs, static_cast<const float4*>(nullptr), static_cast<float4*>(nullptr),
+                 int64_t(0)) != cudaSuccess)
     return MOEX_ECUDA;
   const PfSmem L;
   const PfKernel k1 = pf_kernel<1>(cl, gu->fmt);
@@ -1524,6 +1565,9 @@ moex_status launch_moe_prefill(const moex_qweight* gu, const moex_qweight* dn, c
   g1.ntiles = tl.n1;
   g1.Hs = hs;
   g1.I = I;
+  g1.init_out = reinterpret_cast<float4*>(out);
+  g1.init_res = reinterpret_cast<const float4*>(residual);
+  g1.init_vec4 = static_cast<int64_t>(T) * H / 4;
   g1.status = status;
   if (launch_pf_gemm(k1, cl, L.total, s, m1, q1, s1, g1) != cudaSuccess) return MOEX_ECUDA;
   GemmArgs g2 = {};
@@ -1608,7 +1652,7 @@ moex_status launch_moe_prefill_q8(const moex_qweight* gu, const moex_qweight* dn
   if (launch_pdl(prefill_scan_kernel, dim3(1), dim3(1024), 0, s, n, E, hist, counts, eoff, etb, tl) != cudaSuccess)
     return MOEX_ECUDA;
   const int64_t max_tiles = (static_cast<int64_t>(n) / PF_CAP_ONE + E + 1) * tl.F1;
-  if (launch_pdl(prefill_tiles_kernel, dim3(static_cast<unsigned>((max_tiles + 255) / 256)), dim3(256), 0, s, E,
+  if (launch_pdl(prefill_tiles_kernel, dim3(static_cast<unsigned>((max_tiles + 255) / 256)), dim3(256), esm + 4, s, E,
                  static_cast<const int*>(counts), static_cast<const int*>(eoff), static_cast<const int*>(etb),
                  tl) != cudaSuccess)
     return MOEX_ECUDA;
