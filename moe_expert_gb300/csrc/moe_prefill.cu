@@ -623,10 +623,10 @@ __device__ __forceinline__ int pf_gu_raw_row(int m) {
 // PAIR: CTA pairs (clusters of two) on neighbouring feature tiles of the same
 // token tile share M = 256 MMAs (tcgen05 cta_group::2): each CTA dequantises
 // its own 128 weight rows into its own TMEM and loads its own half of the
-// token rows with plain TMA, so every SM writes and the MMA reads half of the
-// tile's token bytes per k-step; the even CTA issues the MMAs and commits them
-// to the barriers of both CTAs, and a forwarding thread of the odd CTA tells
-// it when that CTA's half of a stage is in place.  A pair's tile has up to
+// token rows with TMA (no multicast), so every SM writes and the MMA reads
+// half of the tile's token bytes per k-step; both CTAs' loads count their
+// bytes on the even CTA's stage barrier (cta_group::2 loads), and the even
+// CTA issues the MMAs and commits them to the barriers of both CTAs.  A pair's tile has up to
 // 384 tokens in two sub-tiles (two accumulator slots), so each dequantised
 // weight stage feeds twice the MMA work of a 192-token tile.  !PAIR: one CTA,
 // M = 128, tiles of up to 192 tokens.
@@ -648,9 +648,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   // k-step kc uses B stage kc % NB and A stage kc % PF_NA_ST; its one
   // MMA commit (for a pair, to both CTAs) completes kdone[kc % PF_KD], which
   // frees both stages
-  uint64_t* b_full = bars;                  // this CTA's B stage has landed
-  uint64_t* b_peer = b_full + NB;     // (issuing CTA of a pair) the odd CTA's B stage has landed
-  uint64_t* kdone = b_peer + NB;
+  // b_full[s]: the B stage has landed (for a pair, on the issuing CTA: both
+  // CTAs' halves, whose loads both count their bytes on it)
+  uint64_t* b_full = bars;
+  uint64_t* kdone = b_full + NB;
   // full[s] (on the CTA that issues the MMAs): the A stage is in TMEM in
   // every CTA of the pair (each dequantising warp arrives; the odd CTA's
   // remotely)
@@ -668,10 +669,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NB; ++i) {
-      mbar_init(&b_full[i], 1);
-      mbar_init(&b_peer[i], 1);     // the odd CTA's forwarder
-    }
+    for (int i = 0; i < NB; ++i) mbar_init(&b_full[i], 1);
     for (int i = 0; i < PF_KD; ++i) mbar_init(&kdone[i], 1);  // the MMA thread's commit
     for (int i = 0; i < PF_NA_ST; ++i) mbar_init(&full[i], PAIR ? 2 * PF_DQ_WARPS : PF_DQ_WARPS);
     for (int i = 0; i < 2; ++i) {
@@ -718,6 +716,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
   if (warp == 0) {
     // ------------------------------------------------ B producer (TMA of this CTA's token rows)
     if (lane == 0) {
+      const uint32_t b_full_mma = PAIR ? cluster_addr(smem_u32(b_full), 0) : 0u;
       int kc = 0;
       int4 nxt = t0 < ntiles ? a.tiles[t0] : make_int4(0, 0, 0, 0);
       for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
@@ -727,7 +726,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
         int src[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) src[h] = tile.z + st.start[h] + (PAIR ? rank * (st.n[h] / 2) : 0);
-        const uint32_t half_bytes = (st.nbox[0] + st.nbox[1]) * BOXR * PF_BOXK * 2;
+        const uint32_t half_bytes = (st.nbox[0] + st.nbox[1]) * BOXR * PF_BOXK * 2;  // one CTA's
         for (int ks = 0; ks < KS; ++ks, ++kc) {
           const int s = kc % NB;
           const int j0 = kc - NB;  // the k-step that used this stage before
@@ -737,41 +736,36 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
             break;
           }
           const int nhalf = (half_last && ks == KS - 1) ? 1 : 2;
-          mbar_arrive_expect_tx(&b_full[s], nhalf * half_bytes);
+          // a pair's two CTAs load the same number of boxes
+          if (rank == 0) mbar_arrive_expect_tx(&b_full[s], (PAIR ? 2 : 1) * nhalf * half_bytes);
           for (int j = 0; j < nhalf; ++j)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-              for (int bx = 0; bx < st.nbox[h]; ++bx)
-                tma_load_2d(sb + s * STAGE_B + j * HALF_B + (st.off[h] + bx * BOXR) * PF_BOXK * 2, &bmap,
-                            ks * PF_BK + j * PF_BOXK, src[h] + BOXR * bx, &b_full[s]);
+              for (int bx = 0; bx < st.nbox[h]; ++bx) {
+                uint8_t* dst = sb + s * STAGE_B + j * HALF_B + (st.off[h] + bx * BOXR) * PF_BOXK * 2;
+                if constexpr (PAIR)
+                  tma_load_2d_pair(dst, &bmap, ks * PF_BK + j * PF_BOXK, src[h] + BOXR * bx, b_full_mma + 8u * s);
+                else
+                  tma_load_2d(dst, &bmap, ks * PF_BK + j * PF_BOXK, src[h] + BOXR * bx, &b_full[s]);
+              }
         }
       }
-      // after an abort, let the copies already issued land before the CTA exits
+      // after an abort, let the copies already issued land before the CTA
+      // exits: the issuing CTA waits for its stages (which count the odd
+      // CTA's bytes too); the odd CTA, which cannot wait on that barrier,
+      // gives its copies a fixed 100 us
       if (*abort_flag) {
-        for (int j = kc - 1; j >= 0 && j >= kc - NB; --j)
-          mbar_wait(&b_full[j % NB], (j / NB) & 1, nullptr);
+        if (rank == 0) {
+          for (int j = kc - 1; j >= 0 && j >= kc - NB; --j)
+            mbar_wait(&b_full[j % NB], (j / NB) & 1, nullptr);
+        } else {
+          const uint64_t t_ab = global_timer_ns();
+          while (global_timer_ns() - t_ab < 100000ull) __nanosleep(1000);
+        }
       }
     }
   } else if (warp == 1 && PAIR && rank == 1) {
-    // ------------------------------------------------ odd CTA of a pair: B stage forwarder
-    // once this CTA's B stage (its half of the token rows) has landed, tell
-    // the even CTA, whose MMA reads it (the A stage is announced by the
-    // dequantising warps themselves)
-    if (lane == 0) {
-      const uint32_t peer_b = cluster_addr(smem_u32(b_peer), 0);
-      int kc = 0;
-      for (int t = t0; t < ntiles && !*abort_flag; t += tstep) {
-        for (int ks = 0; ks < KS; ++ks, ++kc) {
-          const int s = kc % NB;
-          if (!mbar_wait(&b_full[s], (kc / NB) & 1, abort_flag)) {
-            *abort_flag = 1;
-            flag_status(a.status, DEV_TIMEOUT_MMA);
-            break;
-          }
-          mbar_arrive_remote(peer_b + 8u * s);
-        }
-      }
-    }
+    // the odd CTA of a pair issues no MMAs
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (one CTA, or the even CTA of a pair)
     if (lane == 0) {
@@ -814,7 +808,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const __gri
         for (int ks = 0; ks < KS; ++ks, ++kc) {
           const int sb_ = kc % NB, sa = kc % PF_NA_ST;
           if (!mbar_wait(&b_full[sb_], (kc / NB) & 1, abort_flag) ||
-              (PAIR && !mbar_wait(&b_peer[sb_], (kc / NB) & 1, abort_flag)) ||
               !mbar_wait(&full[sa], (kc / PF_NA_ST) & 1, abort_flag)) {
             *abort_flag = 1;
             flag_status(a.status, DEV_TIMEOUT_MMA);
