@@ -111,12 +111,13 @@ __device__ __forceinline__ void load_act(ActRegs<FMT, C>& r, const int8_t* const
 // Integer dots of one weight block with C columns, then
 // p[c] = I * (dw * dx[c]) in FP32.  The block's quant bytes are given as
 // 16-byte chunks q0 (and q1 for Q8_0).
-template <int FMT, int C>
+// SPLIT (IQ4_NL, C <= 2): two table lookups and two dp4a's per four weights
+// (split codebook) instead of rebuilding the values: fewer instructions, but
+// twice the dp4a's.
+template <int FMT, int C, bool SPLIT = false>
 __device__ __forceinline__ void block_dots_from(uint4 q0, uint4 q1, float dw, const ActRegs<FMT, C>& act, float* p,
                                                 int* I_out = nullptr) {
-  if constexpr (FMT != MOEX_Q8_0 && C <= 2) {
-    // one or two columns: two table lookups and two dp4a's per four weights
-    // (split codebook) cost fewer instructions than rebuilding the values
+  if constexpr (FMT != MOEX_Q8_0 && C <= 2 && SPLIT) {
     (void)q1;
     const uint32_t W[4] = {q0.x, q0.y, q0.z, q0.w};
     int I[C];
@@ -173,7 +174,7 @@ __device__ __forceinline__ void block_row_dots(const uint8_t* wq, float dw, cons
   const int o0 = swap ? 16 : 0;
   const uint4 q0 = *reinterpret_cast<const uint4*>(wq + o0);
   const uint4 q1 = FMT == MOEX_Q8_0 ? *reinterpret_cast<const uint4*>(wq + (16 - o0)) : q0;
-  block_dots_from<FMT, C>(q0, q1, dw, act, p, I_out);
+  block_dots_from<FMT, C, true>(q0, q1, dw, act, p, I_out);
 }
 
 // Shared-memory reads of Q8_0 blocks: lane li of a half warp reads its
