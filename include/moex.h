@@ -243,8 +243,9 @@ moex_status moex_moe_prefill_workspace_layout(int T, int k, int E, int64_t hidde
  *            moex_route_topk); out : device FP32 [T][hidden] (overwritten).
  *   ws     : device workspace of moex_moe_prefill_workspace_bytes() bytes.
  * hidden % 128 == 0, inter % 64 == 0, E <= 4096, E * 2 * inter < 2^31.
- * Seven launches (sort: histogram, scan, tiles, scatter; gather, which also
- * clears out; GEMM 1; GEMM 2); the GEMMs use tcgen05 / TMEM / TMA.  An
+ * Seven launches (sort: histogram, scan, tiles, scatter; gather; GEMM 1,
+ * whose epilogue warps also clear out; GEMM 2); the GEMMs use tcgen05 / TMEM
+ * / TMA.  An
  * entry whose id is outside [0, E) is left out of the layer and flagged
  * (MOEX_EDEVICE).
  */
