@@ -551,7 +551,7 @@ struct PfSmem {
     int o = 0;
     b = o; o += PF_B_BYTES;                                     // 1024-aligned (dynamic smem base)
     raw = o; o += PF_NR_ST * PF_RAW_STAGE;                      // 1024-aligned
-    bars = o; o += 8 * (2 * PF_NB_MAX + PF_KD + PF_NA_ST + 2 * PF_NR_ST + 4 + 1);
+    bars = o; o += 8 * (PF_NB_MAX + PF_KD + PF_NA_ST + 2 * PF_NR_ST + 4 + 1);  // b_full, kdone, full, d_full/d_empty, done, r_full/r_empty
     o = (o + 15) & ~15;
     xch = o; o += 4 * 2 * 2 * 32 * 4;                          // integer route: per warp pair, amax and sums of 32 columns
     tmem = o; o += 16;
