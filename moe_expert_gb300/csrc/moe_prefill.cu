@@ -95,12 +95,23 @@ struct PrefillTiles {
 // An expert's n rows are cut into ceil(n / cap) token tiles of balanced size
 // (the first n % nt tiles one row longer), so every tile of an expert does
 // about the same MMA work per dequantised weight stage.
-__host__ __device__ inline int pf_token_tiles(int n, int cap) { return (n + cap - 1) / cap; }
+// Token tiles of n rows with at most cap rows (a multiple of 16) each: the
+// fewest tiles, all but the last of the same size, that size a multiple of
+// 16 (the MMA's N granularity), so the padding of a whole expert is under 16
+// rows rather than under 16 rows a tile.
+__host__ __device__ inline int pf_tile_rows(int n, int cap) {
+  const int nt = (n + cap - 1) / cap;
+  return (((n + nt - 1) / nt) + 15) & ~15;
+}
+__host__ __device__ inline int pf_token_tiles(int n, int cap) {
+  if (n <= 0) return 0;
+  const int b = pf_tile_rows(n, cap);
+  return (n + b - 1) / b;
+}
 __host__ __device__ inline void pf_tile_span(int n, int cap, int t, int* r0, int* rows) {
-  const int nt = pf_token_tiles(n, cap);
-  const int base = n / nt, rem = n % nt;
-  *r0 = t * base + (t < rem ? t : rem);
-  *rows = base + (t < rem ? 1 : 0);
+  const int b = pf_tile_rows(n, cap);
+  *r0 = t * b;
+  *rows = n - t * b < b ? n - t * b : b;
 }
 
 constexpr int PF_MAX_SEGS = 1024;   // at most this many histogram segments
@@ -266,8 +277,8 @@ __global__ void __launch_bounds__(1024) prefill_scan_kernel(int n, int E, int* _
 }
 
 // Both tile lists, one thread per tile: token tile g belongs to the last
-// expert e with etb[e] <= g; its ceil(n_e / cap) token tiles split the
-// expert's rows evenly.  etb[0..E] is staged in shared memory (E + 1 ints)
+// expert e with etb[e] <= g; its token tiles (pf_tile_span) cut the
+// expert's rows into tiles of a multiple of 16 rows.  etb[0..E] is staged in shared memory (E + 1 ints)
 // for the binary search.
 __global__ void __launch_bounds__(256) prefill_tiles_kernel(int E, const int* __restrict__ counts,
                                                             const int* __restrict__ eoff, const int* __restrict__ etb,
@@ -295,7 +306,7 @@ __global__ void __launch_bounds__(256) prefill_tiles_kernel(int E, const int* __
   (first ? tl.t1 : tl.t2)[j] = make_int4(e, f, eoff[e] + r0, rows);
 }
 
-// Dense product: balanced token tiles of at most `cap` rows times feature
+// Dense product: token tiles (pf_tile_span) of at most `cap` rows times feature
 // tiles of 128 rows, all of matrix 0; n1[0] = tiles, n1[2] = rows.
 __global__ void __launch_bounds__(256) dense_tiles_kernel(int T, int F, int cap, int4* __restrict__ tiles,
                                                           int* __restrict__ n1) {
