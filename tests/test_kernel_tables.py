@@ -3,7 +3,9 @@
 The kernels decode 4-bit indices with `prmt` byte selection from constant
 tables in csrc/common.cuh.  This test emulates `prmt` (default mode: selector
 nibble bits 0-2 pick one of 8 bytes, bit 3 replicates that byte's sign bit)
-and checks both decodings against the codebook fixture for every index.
+and checks every decoding against the codebook fixture for every index: the
+GEMV's rebuilt lookup, the split lookup of the one- and two-column dots, and
+the prefill dequantiser's biased lookup (codebook value + 128).
 """
 
 import os
@@ -18,11 +20,11 @@ def _codebook():
     return [int(v) for v in rows[0].split()]
 
 
-def _constants():
-    with open(os.path.join(ROOT, "moe_expert_gb300", "csrc", "common.cuh")) as f:
+def _constants(name="common.cuh", prefix="IQ4NL_"):
+    with open(os.path.join(ROOT, "moe_expert_gb300", "csrc", name)) as f:
         src = f.read()
     return {m.group(1): int(m.group(2), 16)
-            for m in re.finditer(r"constexpr uint32_t (IQ4NL_\w+) = 0x([0-9A-Fa-f]+)u;", src)}
+            for m in re.finditer(r"constexpr uint32_t (%s\w+) = 0x([0-9A-Fa-f]+)u;" % prefix, src)}
 
 
 def _prmt_byte(a, b, nib):
@@ -54,3 +56,12 @@ def test_iq4nl_split_lookup_sums_to_codebook():
         assert lo + hi == cb[idx], idx
         # each part alone stays an int8 that dp4a reads as signed
         assert -128 <= lo <= 127 and -128 <= hi <= 127
+
+
+def test_iq4nl_biased_lookup_is_codebook_plus_128():
+    cb, k = _codebook(), _constants("moe_prefill.cu", "IQ4B_")
+    for idx in range(16):
+        lo = _prmt_byte(k["IQ4B_LO_0"], k["IQ4B_LO_1"], idx)
+        hi7 = _prmt_byte(k["IQ4B_HI_0"], k["IQ4B_HI_1"], idx ^ 8)
+        b7 = (hi7 + 0x7F) & 0x80
+        assert (lo | hi7 | b7) == cb[idx] + 128, idx
