@@ -14,14 +14,14 @@
 //
 // GB300 design (not the pages' wmma kernels): the weights are the MMA's A
 // operand and live in tensor memory: eight warps dequantise 128 weight rows x
-// 64 inputs per k-step straight from the IQ4_NL (or Q8_0) planes into TMEM
+// 128 inputs per k-step straight from the IQ4_NL (or Q8_0) planes into TMEM
 // with tcgen05.st (one thread per row, no shared-memory round trip); the
 // sorted token rows are the B operand, boxes of a 2-D TMA tensor map with the
 // 128-byte swizzle; tcgen05.mma (K = 16, N = tile tokens rounded up) into a
 // double-buffered FP32 accumulator in TMEM, read back by eight epilogue warps
 // with tcgen05.ld.  Because the token count of an expert is the MMA's N,
-// ragged experts cost a few padded columns per tile instead of a partial
-// 128-row M tile.  CTAs run in pairs (clusters of two) on neighbouring
+// a ragged expert costs at most 15 padded columns (its tiles are multiples
+// of 16 rows but the last) instead of a partial 128-row M tile.  CTAs run in pairs (clusters of two) on neighbouring
 // feature tiles of the same token tile and share M = 256 MMAs (tcgen05
 // cta_group::2): each CTA loads only its half of the token rows, so the
 // shared-memory traffic of the B operand per SM is halved.
